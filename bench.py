@@ -1,0 +1,480 @@
+"""Benchmark of the SP boundary hot path on GB300.
+
+One step = one pass of the whole boundary over one batch: the fused forward
+(g* reduce-scatter + bias + dropout + residual + LayerNorm + g all-gather)
+and the backward (norm / dropout backward, all-gather of the partials'
+gradient, parameter gradients), on the 70B-shape workload (t = 8 emulated
+ranks, b = 1, s = 16384, h = 8192, bf16).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on bounded samples of the same workload.
+
+Launch: ``python bench.py [--gpus N] [--steps K] [--warmup W]``; for N > 1
+under torch.distributed.run, each rank processes its own batch (weak
+scaling, no collective on the data path).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sp_boundary_norm_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "SP-boundary fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak) at h=8192,t=8"
+UNIT = "tokens/s"
+FWD_SOURCES = ("sp_boundary_norm_gb300/csrc/fwd.cu", "sp_boundary_norm_gb300/csrc/sp_device.cuh",
+               "sp_boundary_norm_gb300/csrc/sp_internal.h")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "rs_norm_fwd_kernel_70b.md")
+
+
+# ------------------------------------------------------------ byte counts --
+
+def fwd_bytes_per_token(t, h, n_gather, norm="layernorm"):
+    """Algorithmic bytes: t partials + residual read; Z, mask, O copies, stats written."""
+    stats = 8 if norm == "layernorm" else 4
+    return 2 * t * h + 2 * h + 2 * h + h + 2 * h * n_gather + stats
+
+
+def bwd_bytes_per_token(h, n_gather, norm="layernorm", skip=False):
+    """Algorithmic bytes: dY, Z, mask, stats (+skip) read; dResidual, dYpre copies written."""
+    stats = 8 if norm == "layernorm" else 4
+    return 2 * h + 2 * h + h + stats + (2 * h if skip else 0) + 2 * h + 2 * h * n_gather
+
+
+# ---------------------------------------------------------- distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world, device=None):
+    if world > 1:
+        if device is not None and device.type == "cuda":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def max_over_ranks(value, world, device):
+    """The maximum of a float over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return value
+    x = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+    return float(x.item())
+
+
+# --------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.lines = []
+        ident = None
+        try:
+            ident = str(torch.cuda.get_device_properties(device).uuid)
+            if not ident.startswith("GPU-"):
+                ident = "GPU-" + ident
+        except Exception:
+            ident = None
+        self.ident = ident
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.ident:
+            cmd += ["-i", self.ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0, t1):
+        samples = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            samples.append((ts, sm, smax, parts[5:9]))
+        inside = [s for s in samples if t0 - 0.06 <= s[0] <= t1 + 0.06] or samples
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def clocks_rejected(c):
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if any(r in bad for r in c.get("reasons", [])):
+        return True
+    if c.get("sm_mhz") and c.get("sm_max_mhz") and not c["reasons"]:
+        return c["sm_mhz"] < 0.6 * c["sm_max_mhz"]
+    return False
+
+
+# ----------------------------------------------------------- our arm ------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def fwd_source_sha():
+    h = hashlib.sha256()
+    for rel in FWD_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it is current."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in text.splitlines():
+        if "=" in ln and ln.strip().startswith(("traffic_per_launch_bytes", "source_sha")):
+            k, v = ln.split("=", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha") != fwd_source_sha():
+        return None
+    try:
+        return int(vals["traffic_per_launch_bytes"])
+    except (KeyError, ValueError):
+        return None
+
+
+class Step:
+    """Device buffers and the fwd + bwd calls of one step."""
+
+    def __init__(self, w, device, n_gather=1):
+        from sp_boundary_norm_gb300 import binding as sp
+        self.sp, self.w, self.dev = sp, w, device
+        self.inp = wl.forward_inputs(w, device)
+        self.dy = wl.backward_inputs(w, device)["dy"]
+        sizes = w.shard_sizes()
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        self.z = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+        self.mask = [e((w.b, n, w.h), torch.uint8) for n in sizes]
+        self.mean = [e((w.b, n), torch.float32) for n in sizes]
+        self.rstd = [e((w.b, n), torch.float32) for n in sizes]
+        self.gathered = [e((w.b, w.s, w.h), torch.bfloat16) for _ in range(n_gather)]
+        self.dres = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+        self.dgat = [e((w.b, w.s, w.h), torch.bfloat16) for _ in range(n_gather)]
+        self.dgamma, self.dbeta, self.dbias = (e((w.h,), torch.float32) for _ in range(3))
+        self.ws = e((sp.sp_norm_bwd_workspace_bytes(w.b, w.s, w.h, w.t),), torch.uint8)
+        self.cu = (torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(device) if w.ragged else None)
+
+    def fwd(self):
+        w, i = self.w, self.inp
+        self.sp.sp_rs_norm_fwd(i["partials"], i["residual"], i["bias"], i["gamma"], i["beta"],
+                               eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                               cu_seqlens=self.cu, z_out=self.z, mask_out=self.mask, mean_out=self.mean,
+                               rstd_out=self.rstd, gathered=self.gathered)
+
+    def bwd(self):
+        w = self.w
+        self.sp.sp_norm_bwd(self.dy, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"],
+                            None, s=w.s, p=w.p, norm=w.norm, cu_seqlens=self.cu,
+                            dresidual=self.dres,
+                            dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
+                            dbias=self.dbias, workspace=self.ws)
+
+
+def time_device(step, steps, warmup, world, device):
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        step.fwd()
+        step.bwd()
+    torch.cuda.synchronize(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, end = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+    sampler = ClockSampler(device)
+    sampler.start()
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    start.record(stream)
+    for k in range(steps):
+        ev[k][0].record(stream)
+        step.fwd()
+        ev[k][1].record(stream)
+        step.bwd()
+        ev[k][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    barrier(world, device)
+    sampler.stop()
+    step.sp.check_device_status(device)
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    return total_ms, fwd_ms, bwd_ms, sampler.summary(t0, t1)
+
+
+def time_e2e(step, steps, device):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in and the step's results copied out inside the timed region."""
+    stream = torch.cuda.current_stream(device)
+    host_in = [x.cpu().pin_memory() for x in step.inp["partials"] + step.inp["residual"] + step.dy]
+    dev_in = step.inp["partials"] + step.inp["residual"] + step.dy
+    dev_out = step.gathered + step.dres + step.dgat + [step.dgamma, step.dbeta, step.dbias]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in dev_out]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step.fwd()
+        step.bwd()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    return start.elapsed_time(end), h2d, d2h
+
+
+def cpu_baseline(w, seconds=10.0, n_tokens=64):
+    """The CPU oracle (as it stands) on bounded samples of the workload."""
+    import numpy as np
+    from oracle import boundary as ob
+    sample = w.with_(s=max(w.t, n_tokens // w.t * w.t), name=w.name + "-sample")
+    f = lambda x: x.float().numpy()
+    done, elapsed, reps = 0, 0.0, 0
+    while elapsed < seconds and reps < 1000:
+        inp = wl.forward_inputs(sample, "cpu", seed=100 + reps)
+        dy = [f(x) for x in wl.backward_inputs(sample, "cpu", seed=100 + reps)["dy"]]
+        args = ([f(x) for x in inp["partials"]], [f(x) for x in inp["residual"]], f(inp["bias"]),
+                f(inp["gamma"]), f(inp["beta"]))
+        t0 = time.perf_counter()
+        fw = ob.rs_norm_fwd(*args, eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                            n_gather=1)
+        ob.norm_bwd(dy, fw["z"], fw["mask"], fw["mean"], fw["rstd"], args[3], None, p=w.p,
+                    norm=w.norm, n_gather=1)
+        elapsed += time.perf_counter() - t0
+        done += sample.tokens
+        reps += 1
+    del np
+    return {"value": done / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} batches of {sample.tokens} tokens of the {w.name} shape "
+                      f"(t={w.t}, h={w.h}), fwd+bwd, {elapsed:.1f} s, numpy single thread"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    from sp_boundary_norm_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build_library()
+    barrier(world, device)
+    w = wl.WORKLOADS[args.workload]
+    step = Step(w, device, n_gather=args.n_gather)
+    total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world, device)
+    rejected = False
+    if clocks_rejected(clocks):
+        rejected = True
+        total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world,
+                                                       device)
+    total_ms = max_over_ranks(total_ms, world, device)
+    tokens = w.tokens * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    fb = fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) * w.tokens
+    bb = bwd_bytes_per_token(w.h, args.n_gather, w.norm) * w.tokens
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms)
+    peak, peak_kind = measured_peak()
+    step_ms = total_ms / args.steps
+    achieved = fb / (fwd_avg / 1e3) / 1e9
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    e2e_ms, h2d, d2h = time_e2e(step, e2e_steps, device)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, seconds=args.cpu_seconds)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: LayerNorm boundary fwd+bwd, t={w.t} emulated ranks, "
+                               f"b={w.b}, s={w.s}, h={w.h}, p={w.p}, n_gather={args.n_gather}",
+                   "t": w.t, "b": w.b, "s": w.s, "h": w.h, "norm": w.norm, "p": w.p,
+                   "n_gather": args.n_gather,
+                   "l2": "inputs larger than L2 (2.1 GB of partials per step), no flush",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "hbm_gbs": round((fb + bb) / (step_ms / 1e3) / 1e9, 1),
+        "hbm_frac_of_peak": round((fb + bb) / (step_ms / 1e3) / 1e9 / peak, 4),
+        "fwd": {"ms": round(fwd_avg, 4), "gbs": round(achieved, 1),
+                "bytes": fb, "tokens_per_s": round(w.tokens / (fwd_avg / 1e3), 1)},
+        "bwd": {"ms": round(bwd_avg, 4), "gbs": round(bb / (bwd_avg / 1e3) / 1e9, 1),
+                "bytes": bb, "tokens_per_s": round(w.tokens / (bwd_avg / 1e3), 1)},
+        "roofline": {"bound": "hbm", "kernel": "rs_norm_fwd_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": profiled_traffic(), "algorithmic_bytes": fb},
+        "e2e": {"value": round(w.tokens * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rejected:
+        line["clocks_remeasured"] = True
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------ reference arm ----
+
+def run_reference(args):
+    """The oracle timed on the host cores, on bounded samples per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    from oracle import boundary as ob
+    w = wl.WORKLOADS[args.workload]
+    f = lambda x: x.float().numpy()
+
+    def make(n_tok, seed):
+        sample = w.with_(s=n_tok)
+        inp = wl.forward_inputs(sample, "cpu", seed=seed)
+        dy = [f(x) for x in wl.backward_inputs(sample, "cpu", seed=seed)["dy"]]
+        return sample, ([f(x) for x in inp["partials"]], [f(x) for x in inp["residual"]],
+                        f(inp["bias"]), f(inp["gamma"]), f(inp["beta"])), dy
+
+    def one(sample, a, dy):
+        fw = ob.rs_norm_fwd(*a, eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                            n_gather=1)
+        ob.norm_bwd(dy, fw["z"], fw["mask"], fw["mean"], fw["rstd"], a[3], None, p=w.p,
+                    norm=w.norm, n_gather=1)
+
+    # calibrate the per-step sample so the run stays within about a minute
+    probe = make(w.t * 8, 1)
+    t0 = time.perf_counter()
+    one(*probe)
+    per_tok = (time.perf_counter() - t0) / probe[0].tokens
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n_tok = int(max(w.t, min(w.t * 16, budget / per_tok)) // w.t * w.t)
+    for i in range(args.warmup):
+        one(*make(n_tok, 10 + i))
+    elapsed = 0.0
+    for i in range(args.steps):
+        sample, a, dy = make(n_tok, 1000 + i)
+        t0 = time.perf_counter()
+        one(sample, a, dy)
+        elapsed += time.perf_counter() - t0
+    value = n_tok * args.steps / elapsed
+    del np
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: LayerNorm boundary fwd+bwd, t={w.t}, b={w.b}, "
+                               f"s={w.s}, h={w.h}, p={w.p}, n_gather=1 (sampled: {n_tok} "
+                               f"tokens per step)", "t": w.t, "s": w.s, "h": w.h},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n_tok} tokens per step of the {w.name} shape, "
+                                   f"numpy single thread"},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="70b", choices=["70b", "trace4k", "ragged", "tiny"])
+    ap.add_argument("--n-gather", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -68,7 +68,12 @@ def dropout_scale(p):
 
 
 def _norm_rows(z64, gamma, beta, eps, norm):
-    """Token-wise LayerNorm / RMSNorm of rows z64 (n, h), float64 throughout."""
+    """Token-wise LayerNorm / RMSNorm of rows z64 (n, h), float64 throughout.
+
+    Returns (out, mean, rstd, magnitude) where magnitude = |x_hat * gamma| +
+    |beta| is the size of the terms summed into each output (used only to
+    bound the rounding error of a float32 evaluation in tests).
+    """
     h = z64.shape[-1]
     g64 = np.asarray(gamma, dtype=np.float64)
     if norm == LAYERNORM:
@@ -76,13 +81,14 @@ def _norm_rows(z64, gamma, beta, eps, norm):
         centred = z64 - mu[:, None]
         var = (centred * centred).sum(axis=-1) / h
         rstd = 1.0 / np.sqrt(var + eps)
-        out = centred * rstd[:, None] * g64 + np.asarray(beta, dtype=np.float64)
-        return out, mu, rstd
+        scaled = centred * rstd[:, None] * g64
+        b64 = np.asarray(beta, dtype=np.float64)
+        return scaled + b64, mu, rstd, np.abs(scaled) + np.abs(b64)
     if norm == RMSNORM:
         ms = (z64 * z64).sum(axis=-1) / h
         rstd = 1.0 / np.sqrt(ms + eps)
         out = z64 * rstd[:, None] * g64
-        return out, None, rstd
+        return out, None, rstd, np.abs(out)
     raise ValueError(f"unknown norm {norm!r}")
 
 
@@ -107,8 +113,9 @@ def _after_reduce(y, r_rows, token_index, bias, gamma, beta, *, eps, p, seed,
         zf = (d + np.asarray(r_rows, dtype=np.float32)).astype(np.float32)
         z = _bf16.bf16_round(zf)
         z64 = z.astype(np.float64)
-    out64, mu, rstd = _norm_rows(z64, gamma, beta, eps, norm)
+    out64, mu, rstd, mag = _norm_rows(z64, gamma, beta, eps, norm)
     return {
+        "out_magnitude": mag,
         "z": z,
         "mask": keep.astype(np.uint8),
         "mean": None if mu is None else mu.astype(np.float32),
@@ -228,13 +235,17 @@ def backward_rows(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
     if norm == LAYERNORM:
         m1 = dxhat.sum(axis=-1, keepdims=True) / h
         dz = rs * (dxhat - m1 - xhat * m2)
+        mag = rs * (np.abs(dxhat) + np.abs(m1) + np.abs(xhat * m2))
     else:
         dz = rs * (dxhat - xhat * m2)
+        mag = rs * (np.abs(dxhat) + np.abs(xhat * m2))
     if dz_skip is not None:
         dz = dz + np.asarray(dz_skip, dtype=np.float64)
+        mag = mag + np.abs(np.asarray(dz_skip, dtype=np.float64))
     scale = np.float64(dropout_scale(p))
     dypre = dz * np.asarray(mask, dtype=np.float64) * scale
     return {
+        "dz_magnitude": mag,
         "dz": dz,
         "dresidual": _bf16.bf16_round(dz),
         "dypre_exact": dypre,

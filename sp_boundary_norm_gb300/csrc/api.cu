@@ -1,0 +1,568 @@
+// Host side of the C ABI: argument validation, launch-shape choice, launch.
+//
+// Nothing here allocates device memory; every buffer is the caller's.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "sp_internal.h"
+
+namespace spb {
+
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<int> g_inject{SP_OK};
+// Launch-shape overrides for tuning sweeps: [kernel][stages, blocks per SM].
+std::atomic<int> g_tune[2][2] = {{{0}, {0}}, {{0}, {0}}};
+
+sp_status_t fail(sp_status_t code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+sp_status_t fail_cuda(cudaError_t e, const char* where) {
+  return fail(SP_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool take_injected(sp_status_t* out) {
+  const int code = g_inject.exchange(SP_OK);
+  if (code == SP_OK) return false;
+  *out = fail(static_cast<sp_status_t>(code), "injected failure (sp_debug_inject)");
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A list of device byte ranges; outputs must not overlap anything else.
+struct Ranges {
+  struct R {
+    uintptr_t lo, hi;
+    bool out;
+    const char* what;
+    int idx;
+  };
+  std::vector<R> v;
+  void add(const void* p, size_t bytes, bool out, const char* what, int idx) {
+    if (p == nullptr || bytes == 0) return;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    v.push_back({lo, lo + bytes, out, what, idx});
+  }
+  sp_status_t check() const {
+    for (size_t i = 0; i < v.size(); ++i) {
+      if (!v[i].out) continue;
+      for (size_t j = 0; j < v.size(); ++j) {
+        if (i == j) continue;
+        if (v[i].lo < v[j].hi && v[j].lo < v[i].hi)
+          return fail(SP_ERR_OVERLAP, "output %s[%d] overlaps %s[%d]", v[i].what, v[i].idx,
+                      v[j].what, v[j].idx);
+      }
+    }
+    return SP_OK;
+  }
+};
+
+// Shapes common to every entry point.
+sp_status_t check_shape(int64_t b, int64_t s, int64_t h, int32_t t, const int32_t* cu_seqlens,
+                        int32_t n_seqs) {
+  if (t < 1 || t > SP_MAX_RANKS)
+    return fail(SP_ERR_INVALID_ARG, "t = %d outside [1, %d]", t, SP_MAX_RANKS);
+  if (b < 0 || s < 0) return fail(SP_ERR_INVALID_ARG, "negative b or s");
+  if (h < 8 || h % 8 != 0) return fail(SP_ERR_INVALID_ARG, "h = %lld must be a positive multiple of 8", (long long)h);
+  if (h > SP_MAX_HIDDEN)
+    return fail(SP_ERR_UNSUPPORTED, "h = %lld above SP_MAX_HIDDEN = %d", (long long)h, SP_MAX_HIDDEN);
+  if (cu_seqlens != nullptr) {
+    if (b != 1) return fail(SP_ERR_INVALID_ARG, "cu_seqlens requires b == 1 (got %lld)", (long long)b);
+    if (n_seqs < 1) return fail(SP_ERR_INVALID_ARG, "n_seqs = %d must be >= 1", n_seqs);
+    if (!aligned16(cu_seqlens) && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+      return fail(SP_ERR_MISALIGNED, "cu_seqlens not 4-byte aligned");
+  } else if (t > 0 && s % t != 0) {
+    return fail(SP_ERR_INVALID_ARG, "s = %lld not divisible by t = %d (dense shards are even)",
+                (long long)s, t);
+  }
+  const int64_t elems_limit = int64_t(1) << 60;
+  if (b > 0 && s > 0 && (b > elems_limit / s || b * s > elems_limit / h))
+    return fail(SP_ERR_INVALID_ARG, "b*s*h overflows");
+  return SP_OK;
+}
+
+ShardMap make_map(int64_t b, int64_t s, int64_t h, int32_t t) {
+  ShardMap m{};
+  for (int k = 0; k <= t; ++k) m.off[k] = (k * s) / t;
+  for (int k = t + 1; k <= SP_MAX_RANKS; ++k) m.off[k] = s;
+  m.b = b;
+  m.s = s;
+  m.h = h;
+  m.t = t;
+  return m;
+}
+
+int64_t shard_rows(const ShardMap& m, int k) { return m.b * (m.off[k + 1] - m.off[k]); }
+
+// Per-rank pointer arrays: non-NULL and aligned, except that the pointer of a
+// shard with no token (possible when t > s) is never used and may be anything.
+template <typename T>
+sp_status_t check_ptrs(const T* const* arr, int n, const char* what, bool need16,
+                       const ShardMap* shards = nullptr) {
+  if (n > 0 && arr == nullptr) return fail(SP_ERR_INVALID_ARG, "%s array is NULL", what);
+  for (int i = 0; i < n; ++i) {
+    if (shards != nullptr && shard_rows(*shards, i) == 0) continue;
+    if (arr[i] == nullptr) return fail(SP_ERR_INVALID_ARG, "%s[%d] is NULL", what, i);
+    if (need16 ? !aligned16(arr[i]) : (reinterpret_cast<uintptr_t>(arr[i]) & 3u))
+      return fail(SP_ERR_MISALIGNED, "%s[%d] misaligned", what, i);
+  }
+  return SP_OK;
+}
+
+sp_status_t check_vec(const void* p, const char* what) {
+  if (p == nullptr) return fail(SP_ERR_INVALID_ARG, "%s is NULL", what);
+  if (!aligned16(p)) return fail(SP_ERR_MISALIGNED, "%s misaligned", what);
+  return SP_OK;
+}
+
+int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+constexpr size_t kSmemPerSm = 228 * 1024;     // sm_100-class shared memory per SM
+constexpr size_t kSmemPerBlock = 227 * 1024;  // opt-in maximum per block
+constexpr size_t kReserve = 1024;             // per-block reservation
+
+// (threads, chunks) for a row of h channels: every thread owns 8 channels of
+// each chunk of 8*threads channels.
+void row_shape(int64_t h, int* threads, int* maxc) {
+  const int64_t nvec = h / 8;
+  if (nvec <= 64) {
+    *threads = 64;
+    *maxc = 1;
+  } else {
+    *threads = 256;
+    *maxc = pow2_at_least(static_cast<int>((nvec + 255) / 256));
+  }
+}
+
+// Pick (stages, blocks per SM) with the largest per-SM pipeline depth that
+// fits in shared memory, then cap the grid at what is resident.
+LaunchShape pick_shape(const void* (*kernel)(int, int, int), int which, int64_t rows, int64_t h,
+                       size_t stage_bytes, size_t red_bytes, const int* stage_opts, int n_opts,
+                       int default_stages, int default_blocks) {
+  LaunchShape ls{};
+  row_shape(h, &ls.threads, &ls.maxc);
+  int stages = g_tune[which][0].load();
+  int bps = g_tune[which][1].load();
+  if (stages == 0) stages = default_stages;
+  if (bps == 0) bps = default_blocks;
+  // shrink until it fits
+  auto fits = [&](int st, int bp) {
+    const size_t per_block = st * stage_bytes + red_bytes;
+    return per_block <= kSmemPerBlock && bp * (per_block + kReserve) <= kSmemPerSm;
+  };
+  bool ok = false;
+  for (int bp = bps; bp >= 1 && !ok; --bp) {
+    for (int i = 0; i < n_opts && !ok; ++i) {
+      const int st = stage_opts[i];
+      if (st > stages) continue;
+      if (fits(st, bp)) {
+        stages = st;
+        bps = bp;
+        ok = true;
+      }
+    }
+  }
+  if (!ok) {
+    stages = stage_opts[n_opts - 1];
+    bps = 1;
+  }
+  ls.stages = stages;
+  ls.smem = stages * stage_bytes + red_bytes;
+  const void* fn = kernel(ls.threads, ls.maxc, ls.stages);
+  int occ = bps;
+  if (fn != nullptr &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem) ==
+          cudaSuccess) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, ls.threads, ls.smem) ==
+            cudaSuccess &&
+        n > 0 && n < occ)
+      occ = n;
+  }
+  cudaGetLastError();
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * occ;
+  ls.grid = static_cast<int>(rows < cap ? rows : cap);
+  if (ls.grid < 1) ls.grid = 1;
+  return ls;
+}
+
+const int kFwdStages[] = {6, 4, 3, 2};
+const int kBwdStages[] = {8, 4, 2};
+
+LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
+  int threads, maxc;
+  row_shape(h, &threads, &maxc);
+  const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
+  return pick_shape(fwd_kernel, 0, rows, h, stage, 2 * 32 * sizeof(float), kFwdStages, 4,
+                    /*stages=*/6, /*blocks per SM=*/1);
+}
+
+LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip) {
+  int threads, maxc;
+  row_shape(h, &threads, &maxc);
+  const size_t stage = static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + threads * 8;
+  return pick_shape(bwd_kernel, 1, rows, h, stage, 2 * 32 * sizeof(float2), kBwdStages, 3,
+                    /*stages=*/8, /*blocks per SM=*/1);
+}
+
+cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
+  if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem);
+  if (e != cudaSuccess) return e;
+  void* args[] = {params};
+  e = cudaLaunchKernel(fn, dim3(ls.grid), dim3(ls.threads), args, ls.smem, st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace spb
+
+using namespace spb;
+
+extern "C" {
+
+sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* residual,
+                           const void* bias, const void* gamma, const void* beta, int64_t b,
+                           int64_t s, int64_t h, int32_t t, float eps, double p, uint64_t seed,
+                           uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
+                           sp_norm_t norm, void* const* z_out, uint8_t* const* mask_out,
+                           float* const* mean_out, float* const* rstd_out,
+                           void* const* gathered, int32_t n_gather, int32_t* dev_status,
+                           void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
+  if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
+    return fail(SP_ERR_INVALID_ARG, "unknown norm %d", (int)norm);
+  if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SP_ERR_INVALID_ARG, "eps must be > 0");
+  if (!(p >= 0.0 && p < 1.0)) return fail(SP_ERR_INVALID_ARG, "p = %g outside [0, 1)", p);
+  if (n_gather < 0 || n_gather > SP_MAX_RANKS)
+    return fail(SP_ERR_INVALID_ARG, "n_gather = %d outside [0, %d]", n_gather, SP_MAX_RANKS);
+  const bool ln = norm == SP_NORM_LAYERNORM;
+  if (b * s == 0) return SP_OK;   // nothing to read or write: any pointers are fine
+  const ShardMap map = make_map(b, s, h, t);
+  if ((st = check_ptrs(partials, t, "partials", true)) != SP_OK) return st;
+  if ((st = check_ptrs(residual, t, "residual", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(z_out, t, "z_out", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(rstd_out, t, "rstd_out", false, &map)) != SP_OK) return st;
+  if (ln && (st = check_ptrs(mean_out, t, "mean_out", false, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(gathered, n_gather, "gathered", true)) != SP_OK) return st;
+  if ((st = check_vec(bias, "bias")) != SP_OK) return st;
+  if ((st = check_vec(gamma, "gamma")) != SP_OK) return st;
+  if (ln && (st = check_vec(beta, "beta")) != SP_OK) return st;
+  if (dev_status != nullptr && (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
+
+  const size_t full = static_cast<size_t>(b * s * h) * 2;
+  Ranges rg;
+  for (int r = 0; r < t; ++r) rg.add(partials[r], full, false, "partials", r);
+  for (int k = 0; k < t; ++k) {
+    const size_t n = static_cast<size_t>(shard_rows(map, k));
+    rg.add(residual[k], n * h * 2, false, "residual", k);
+    rg.add(z_out[k], n * h * 2, true, "z_out", k);
+    rg.add(mask_out[k], n * h, true, "mask_out", k);
+    rg.add(rstd_out[k], n * 4, true, "rstd_out", k);
+    if (ln) rg.add(mean_out[k], n * 4, true, "mean_out", k);
+  }
+  for (int j = 0; j < n_gather; ++j) rg.add(gathered[j], full, true, "gathered", j);
+  rg.add(bias, h * 2, false, "bias", 0);
+  rg.add(gamma, h * 2, false, "gamma", 0);
+  if (ln) rg.add(beta, h * 2, false, "beta", 0);
+  if ((st = rg.check()) != SP_OK) return st;
+
+  const int64_t rows = b * s;
+  if (rows == 0) return SP_OK;
+
+  FwdParams P{};
+  P.map = map;
+  for (int r = 0; r < t; ++r) P.partials[r] = static_cast<const uint16_t*>(partials[r]);
+  for (int k = 0; k < t; ++k) {
+    P.residual[k] = static_cast<const uint16_t*>(residual[k]);
+    P.z[k] = static_cast<uint16_t*>(z_out[k]);
+    P.mask[k] = mask_out[k];
+    P.rstd[k] = rstd_out[k];
+    P.mean[k] = ln ? mean_out[k] : nullptr;
+  }
+  for (int j = 0; j < n_gather; ++j) P.gathered[j] = static_cast<uint16_t*>(gathered[j]);
+  P.bias = static_cast<const uint16_t*>(bias);
+  P.gamma = static_cast<const uint16_t*>(gamma);
+  P.beta = ln ? static_cast<const uint16_t*>(beta) : nullptr;
+  P.cu_seqlens = cu_seqlens;
+  P.n_seqs = n_seqs;
+  P.n_gather = n_gather;
+  P.norm = norm;
+  // keep iff draw >= floor(p * 2^32): the drop probability is thr / 2^32
+  P.thr = static_cast<uint32_t>(std::floor(p * 4294967296.0));
+  P.scale = static_cast<float>(1.0 / (1.0 - p));
+  P.eps = eps;
+  P.key0 = static_cast<uint32_t>(seed);
+  P.key1 = static_cast<uint32_t>(seed >> 32);
+  P.off0 = static_cast<uint32_t>(offset);
+  P.off1 = static_cast<uint32_t>(offset >> 32);
+  P.rows = rows;
+  P.status = dev_status;
+
+  const LaunchShape ls = fwd_shape(rows, h, t);
+  const cudaError_t e = launch(fwd_kernel(ls.threads, ls.maxc, ls.stages), ls, &P,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_fwd launch");
+  return SP_OK;
+}
+
+static sp_status_t seq_copy_common(const void* const* src, int n_src, const char* src_name,
+                                   bool src_full, void* const* dst, int n_dst,
+                                   const char* dst_name, bool dst_full, int64_t b, int64_t s,
+                                   int64_t h, int32_t t, const int32_t* cu_seqlens,
+                                   int32_t n_seqs, int32_t* dev_status, CopyParams* P) {
+  sp_status_t st;
+  if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
+  *P = CopyParams{};
+  P->rows = b * s;
+  if (P->rows == 0) return SP_OK;   // nothing to copy: any pointers are fine
+  const ShardMap map = make_map(b, s, h, t);
+  if ((st = check_ptrs(src, n_src, src_name, true, src_full ? nullptr : &map)) != SP_OK) return st;
+  if ((st = check_ptrs(dst, n_dst, dst_name, true, dst_full ? nullptr : &map)) != SP_OK) return st;
+  if (dev_status != nullptr && (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
+  const size_t full = static_cast<size_t>(b * s * h) * 2;
+  Ranges rg;
+  for (int i = 0; i < n_src; ++i)
+    rg.add(src[i], src_full ? full : shard_rows(map, i) * h * 2, false, src_name, i);
+  for (int i = 0; i < n_dst; ++i)
+    rg.add(dst[i], dst_full ? full : shard_rows(map, i) * h * 2, true, dst_name, i);
+  if ((st = rg.check()) != SP_OK) return st;
+  P->map = map;
+  for (int i = 0; i < n_src; ++i) P->src[i] = static_cast<const uint16_t*>(src[i]);
+  for (int i = 0; i < n_dst; ++i) P->dst[i] = static_cast<uint16_t*>(dst[i]);
+  P->n_dst = n_dst;
+  P->cu_seqlens = cu_seqlens;
+  P->n_seqs = n_seqs;
+  P->status = dev_status;
+  return SP_OK;
+}
+
+sp_status_t sp_allgather_seq(const void* const* shards, int64_t b, int64_t s, int64_t h,
+                             int32_t t, const int32_t* cu_seqlens, int32_t n_seqs,
+                             void* const* gathered, int32_t n_gather, int32_t* dev_status,
+                             void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if (n_gather < 1 || n_gather > SP_MAX_RANKS)
+    return fail(SP_ERR_INVALID_ARG, "n_gather = %d outside [1, %d]", n_gather, SP_MAX_RANKS);
+  CopyParams P;
+  if ((st = seq_copy_common(shards, t, "shards", false, gathered, n_gather, "gathered", true, b,
+                            s, h, t, cu_seqlens, n_seqs, dev_status, &P)) != SP_OK)
+    return st;
+  if (P.rows == 0) return SP_OK;
+  const cudaError_t e = launch_allgather(P, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "sp_allgather_seq launch");
+  return SP_OK;
+}
+
+sp_status_t sp_reduce_scatter_seq(const void* const* partials, int64_t b, int64_t s, int64_t h,
+                                  int32_t t, const int32_t* cu_seqlens, int32_t n_seqs,
+                                  void* const* shards, int32_t* dev_status, void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  CopyParams P;
+  if ((st = seq_copy_common(partials, t, "partials", true, shards, t, "shards", false, b, s, h,
+                            t, cu_seqlens, n_seqs, dev_status, &P)) != SP_OK)
+    return st;
+  if (P.rows == 0) return SP_OK;
+  const cudaError_t e = launch_reduce_scatter(P, t, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "sp_reduce_scatter_seq launch");
+  return SP_OK;
+}
+
+size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, sp_norm_t norm) {
+  (void)norm;
+  if (b <= 0 || s <= 0 || h < 8 || h % 8 != 0 || h > SP_MAX_HIDDEN || t < 1 || t > SP_MAX_RANKS)
+    return 0;
+  // the skip gradient does not change the grid (same threads and occupancy cap)
+  const LaunchShape ls = bwd_shape(b * s, h, false);
+  const LaunchShape ls2 = bwd_shape(b * s, h, true);
+  const int grid = ls.grid > ls2.grid ? ls.grid : ls2.grid;
+  return static_cast<size_t>(grid) * 3 * static_cast<size_t>(h) * sizeof(float);
+}
+
+sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8_t* const* mask,
+                        const float* const* mean, const float* const* rstd, const void* gamma,
+                        const void* const* dz_skip, int64_t b, int64_t s, int64_t h, int32_t t,
+                        double p, const int32_t* cu_seqlens, int32_t n_seqs, sp_norm_t norm,
+                        void* const* dresidual, void* const* dgathered, int32_t n_gather,
+                        float* dgamma, float* dbeta, float* dbias, void* workspace,
+                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
+  if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
+    return fail(SP_ERR_INVALID_ARG, "unknown norm %d", (int)norm);
+  if (!(p >= 0.0 && p < 1.0)) return fail(SP_ERR_INVALID_ARG, "p = %g outside [0, 1)", p);
+  if (n_gather < 0 || n_gather > SP_MAX_RANKS)
+    return fail(SP_ERR_INVALID_ARG, "n_gather = %d outside [0, %d]", n_gather, SP_MAX_RANKS);
+  const bool ln = norm == SP_NORM_LAYERNORM;
+  const int64_t rows = b * s;
+  if (dgamma != nullptr && !aligned16(dgamma)) return fail(SP_ERR_MISALIGNED, "dgamma misaligned");
+  if (dbeta != nullptr && !aligned16(dbeta)) return fail(SP_ERR_MISALIGNED, "dbeta misaligned");
+  if (dbias != nullptr && !aligned16(dbias)) return fail(SP_ERR_MISALIGNED, "dbias misaligned");
+  if (rows == 0) {
+    // no token: the parameter gradients are exact zeros, nothing else is touched
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (dgamma) e = cudaMemsetAsync(dgamma, 0, h * 4, cs);
+    if (e == cudaSuccess && dbeta && ln) e = cudaMemsetAsync(dbeta, 0, h * 4, cs);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, h * 4, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd zero fill");
+    return SP_OK;
+  }
+  const ShardMap map = make_map(b, s, h, t);
+  if ((st = check_ptrs(dy, t, "dy", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(z, t, "z", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(mask, t, "mask", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(rstd, t, "rstd", false, &map)) != SP_OK) return st;
+  if (ln && (st = check_ptrs(mean, t, "mean", false, &map)) != SP_OK) return st;
+  if (dz_skip != nullptr && (st = check_ptrs(dz_skip, t, "dz_skip", true, &map)) != SP_OK)
+    return st;
+  if ((st = check_ptrs(dresidual, t, "dresidual", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(dgathered, n_gather, "dgathered", true)) != SP_OK) return st;
+  if ((st = check_vec(gamma, "gamma")) != SP_OK) return st;
+  if (dev_status != nullptr && (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
+
+  const bool has_skip = dz_skip != nullptr;
+  const LaunchShape ls = bwd_shape(rows, h, has_skip);
+  const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(SP_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(SP_ERR_MISALIGNED, "workspace misaligned");
+
+  const size_t full = static_cast<size_t>(rows * h) * 2;
+  Ranges rg;
+  for (int k = 0; k < t; ++k) {
+    const size_t n = static_cast<size_t>(shard_rows(map, k));
+    rg.add(dy[k], n * h * 2, false, "dy", k);
+    rg.add(z[k], n * h * 2, false, "z", k);
+    rg.add(mask[k], n * h, false, "mask", k);
+    rg.add(rstd[k], n * 4, false, "rstd", k);
+    if (ln) rg.add(mean[k], n * 4, false, "mean", k);
+    if (has_skip) rg.add(dz_skip[k], n * h * 2, false, "dz_skip", k);
+    rg.add(dresidual[k], n * h * 2, true, "dresidual", k);
+  }
+  for (int j = 0; j < n_gather; ++j) rg.add(dgathered[j], full, true, "dgathered", j);
+  rg.add(gamma, h * 2, false, "gamma", 0);
+  rg.add(dgamma, h * 4, true, "dgamma", 0);
+  if (ln) rg.add(dbeta, h * 4, true, "dbeta", 0);
+  rg.add(dbias, h * 4, true, "dbias", 0);
+  rg.add(workspace, need, true, "workspace", 0);
+  if ((st = rg.check()) != SP_OK) return st;
+
+  BwdParams P{};
+  P.map = map;
+  for (int k = 0; k < t; ++k) {
+    P.dy[k] = static_cast<const uint16_t*>(dy[k]);
+    P.z[k] = static_cast<const uint16_t*>(z[k]);
+    P.mask[k] = mask[k];
+    P.rstd[k] = rstd[k];
+    P.mean[k] = ln ? mean[k] : nullptr;
+    P.dz_skip[k] = has_skip ? static_cast<const uint16_t*>(dz_skip[k]) : nullptr;
+    P.dresidual[k] = static_cast<uint16_t*>(dresidual[k]);
+  }
+  for (int j = 0; j < n_gather; ++j) P.dgathered[j] = static_cast<uint16_t*>(dgathered[j]);
+  P.gamma = static_cast<const uint16_t*>(gamma);
+  P.cu_seqlens = cu_seqlens;
+  P.n_seqs = n_seqs;
+  P.n_gather = n_gather;
+  P.norm = norm;
+  P.has_skip = has_skip ? 1 : 0;
+  P.scale = static_cast<float>(1.0 / (1.0 - p));
+  P.rows = rows;
+  P.ws = static_cast<float*>(workspace);
+  P.status = dev_status;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(bwd_kernel(ls.threads, ls.maxc, ls.stages), ls, &P, cs);
+  if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd launch");
+  if (dgamma || (dbeta && ln) || dbias) {
+    ParamReduceParams R{};
+    R.ws = P.ws;
+    R.nblk = ls.grid;
+    R.h = h;
+    R.out[0] = dgamma;
+    R.out[1] = ln ? dbeta : nullptr;
+    R.out[2] = dbias;
+    e = launch_param_reduce(R, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd parameter reduce launch");
+  }
+  return SP_OK;
+}
+
+const char* sp_last_error(void) { return g_err; }
+
+int32_t sp_abi_version(void) { return SP_ABI_VERSION; }
+
+sp_status_t sp_debug_inject(sp_status_t code) {
+  g_inject.store(static_cast<int>(code));
+  return SP_OK;
+}
+
+sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm) {
+  if (kernel < 0 || kernel > 1 || stages < 0 || stages > 8 || blocks_per_sm < 0 ||
+      blocks_per_sm > 8)
+    return fail(SP_ERR_INVALID_ARG, "sp_debug_tune: bad arguments");
+  g_tune[kernel][0].store(stages);
+  g_tune[kernel][1].store(blocks_per_sm);
+  return SP_OK;
+}
+
+sp_status_t sp_debug_philox(const uint32_t* in, uint32_t* out, int64_t n, void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if (n < 0) return fail(SP_ERR_INVALID_ARG, "n < 0");
+  if (n == 0) return SP_OK;
+  if (in == nullptr || out == nullptr) return fail(SP_ERR_INVALID_ARG, "NULL buffer");
+  const cudaError_t e = launch_debug_philox(in, out, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "sp_debug_philox launch");
+  return SP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Unfused sequence-dimension collectives over emulated rank buffers:
+// g (all-gather along s) and g* (reduce-scatter along s) on their own, as in
+// "第 7 课：序列并行 SP" §3.A, plus a device Philox probe for tests.
+//
+// On one GPU a "rank" is a buffer, so an all-gather is a strided copy of
+// each shard into the full buffer(s) and a reduce-scatter reads shard k's
+// rows from all t partials.  Both are pure HBM streams: a persistent grid,
+// one token row per block iteration, 16-byte loads that bypass L1 and
+// streaming 16-byte stores, several loads in flight per thread.
+#include "sp_device.cuh"
+
+namespace spb {
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads) allgather_kernel(const CopyParams P) {
+  if (blockIdx.x == 0 && threadIdx.x < 32)
+    check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
+  const int64_t h = P.map.h;
+  const int64_t nvec = h / 8;
+  for (int64_t row = blockIdx.x; row < P.rows; row += gridDim.x) {
+    int k;
+    int64_t local;
+    locate(P.map, row, k, local);
+    const uint16_t* src = P.src[k] + local * h;
+    for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += kCopyThreads * kCopyUnroll) {
+      uint4 buf[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t v = v0 + u * kCopyThreads;
+        if (v < nvec) buf[u] = ldg16_stream(src + v * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t v = v0 + u * kCopyThreads;
+        if (v < nvec)
+          for (int j = 0; j < P.n_dst; ++j) st16_stream(P.dst[j] + row * h + v * 8, buf[u]);
+      }
+    }
+  }
+}
+
+// shards[k][local] = bf16(sum over r ascending of partials[r][row]), float32.
+__global__ void __launch_bounds__(kCopyThreads) reduce_scatter_kernel(const CopyParams P,
+                                                                      int t) {
+  if (blockIdx.x == 0 && threadIdx.x < 32)
+    check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
+  const int64_t h = P.map.h;
+  const int64_t nvec = h / 8;
+  for (int64_t row = blockIdx.x; row < P.rows; row += gridDim.x) {
+    int k;
+    int64_t local;
+    locate(P.map, row, k, local);
+    uint16_t* dst = P.dst[k] + local * h;
+    for (int64_t v = threadIdx.x; v < nvec; v += kCopyThreads) {
+      const int64_t off = row * h + v * 8;
+      float y[8], q[8];
+      unpack8(ldg16_stream(P.src[0] + off), y);
+      for (int r = 1; r < t; ++r) {
+        unpack8(ldg16_stream(P.src[r] + off), q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], q[e]);
+      }
+      st16_stream(dst + v * 8, pack8(y));
+    }
+  }
+}
+
+__global__ void debug_philox_kernel(const uint32_t* in, uint32_t* out, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t* a = in + 6 * i;
+  const uint4 r = philox4x32_10(make_uint4(a[0], a[1], a[2], a[3]), a[4], a[5]);
+  out[4 * i + 0] = r.x;
+  out[4 * i + 1] = r.y;
+  out[4 * i + 2] = r.z;
+  out[4 * i + 3] = r.w;
+}
+
+static int copy_grid(int64_t rows) {
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  return static_cast<int>(rows < cap ? rows : cap);
+}
+
+cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st) {
+  allgather_kernel<<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_scatter(const CopyParams& p, int t, cudaStream_t st) {
+  reduce_scatter_kernel<<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p, t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_philox(const uint32_t* in, uint32_t* out, int64_t n, cudaStream_t st) {
+  const int64_t blocks = (n + 255) / 256;
+  debug_philox_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace spb

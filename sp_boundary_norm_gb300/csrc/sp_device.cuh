@@ -1,0 +1,233 @@
+// Device helpers for the SP boundary kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sp_internal.h"
+
+namespace spb {
+
+// ----------------------------------------------------------------- Philox --
+// Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3" (SC'11): per round, two 32x32->64-bit
+// multiplies of counter words 0 and 2 by fixed odd multipliers; the high
+// halves are xored with the other two counter words and the round key; the key
+// then advances by the Weyl increments (golden ratio, sqrt(3) - 1).
+constexpr uint32_t kPhiloxMul0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxMul1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxWeyl0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxWeyl1 = 0xBB67AE85u;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0 = static_cast<uint64_t>(kPhiloxMul0) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(kPhiloxMul1) * c.z;
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += kPhiloxWeyl0;
+    k1 += kPhiloxWeyl1;
+  }
+  return c;
+}
+
+// Keep bits of the 8 consecutive elements starting at global element index
+// `e0` (a multiple of 8): element i keeps iff word (i & 3) of Philox at counter
+// (i >> 2, offset) is >= thr.  Bit e of the result is element e0 + e.
+__device__ __forceinline__ uint32_t keep_bits8(uint64_t e0, uint32_t thr, uint32_t k0,
+                                               uint32_t k1, uint32_t off0, uint32_t off1) {
+  const uint64_t q = e0 >> 2;
+  const uint4 a = philox4x32_10(
+      make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), off0, off1), k0, k1);
+  const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+                                           static_cast<uint32_t>((q + 1) >> 32), off0, off1),
+                                k0, k1);
+  return (a.x >= thr ? 1u : 0u) | (a.y >= thr ? 2u : 0u) | (a.z >= thr ? 4u : 0u) |
+         (a.w >= thr ? 8u : 0u) | (b.x >= thr ? 16u : 0u) | (b.y >= thr ? 32u : 0u) |
+         (b.z >= thr ? 64u : 0u) | (b.w >= thr ? 128u : 0u);
+}
+
+// ------------------------------------------------------------------- bf16 --
+__device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16);
+  f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16);
+  f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// 8 mask bytes (0/1) from 8 keep bits.
+__device__ __forceinline__ uint2 bits_to_bytes8(uint32_t bits) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    lo |= ((bits >> e) & 1u) << (8 * e);
+    hi |= ((bits >> (e + 4)) & 1u) << (8 * e);
+  }
+  return make_uint2(lo, hi);
+}
+
+// 8 keep bits from 8 mask bytes (any nonzero byte = kept).
+__device__ __forceinline__ uint32_t bytes8_to_bits(uint2 m) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    bits |= (((m.x >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << e;
+    bits |= (((m.y >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << (e + 4);
+  }
+  return bits;
+}
+
+// ----------------------------------------------------- memory primitives --
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared asynchronous copy, L1 bypassed.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst_smem)),
+               "l"(src_gmem)
+               : "memory");
+}
+
+// 8-byte global -> shared asynchronous copy.
+__device__ __forceinline__ void cp_async8(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(dst_smem)),
+               "l"(src_gmem)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds8(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
+  return v;
+}
+
+// Read-only global load through the non-coherent path (small replicated
+// parameters: stays in L1 across rows).
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Streamed (read-once) global load: not allocated in L1.
+__device__ __forceinline__ uint4 ldg16_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Streaming (write-once) global stores.
+__device__ __forceinline__ void st16_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st8_stream(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};\n" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// -------------------------------------------------------------- reductions --
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, m);
+  return v;
+}
+
+// Block-wide sum in a fixed order (deterministic).  `red` is a 32-float
+// shared slot; two consecutive calls must use different slots.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int i = 0; i < nw; ++i) s += red[i];
+  return s;
+}
+
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (lane == 0) red[warp] = make_float2(a, b);
+  __syncthreads();
+  float2 s = make_float2(0.f, 0.f);
+  for (int i = 0; i < nw; ++i) {
+    s.x += red[i].x;
+    s.y += red[i].y;
+  }
+  return s;
+}
+
+// ------------------------------------------------------------- shard map --
+// Token `row` = bi*s + si of the (b, s) grid -> its shard k and its row index
+// inside shard k's (b, s_k) tensor.
+__device__ __forceinline__ void locate(const ShardMap& m, int64_t row, int& k, int64_t& local) {
+  int64_t bi = 0, si = row;
+  if (m.b > 1) {
+    bi = row / m.s;
+    si = row - bi * m.s;
+  }
+  int kk = static_cast<int>((si * m.t) / m.s);
+  if (kk > m.t - 1) kk = m.t - 1;
+  while (kk + 1 < m.t && m.off[kk + 1] <= si) ++kk;
+  while (kk > 0 && m.off[kk] > si) --kk;
+  k = kk;
+  local = bi * (m.off[kk + 1] - m.off[kk]) + (si - m.off[kk]);
+}
+
+// Device check of packed-sequence metadata: cu_seqlens[0] == 0, non-decreasing,
+// cu_seqlens[n] == total.  Run by one warp; flags SP_ERR_DEVICE_CHECK.
+__device__ __forceinline__ void check_cu_seqlens(const int32_t* cu, int32_t n, int64_t total,
+                                                 int32_t* status) {
+  if (cu == nullptr) return;
+  bool bad = false;
+  for (int i = threadIdx.x & 31; i <= n; i += 32) {
+    const int32_t v = cu[i];
+    if (i == 0 && v != 0) bad = true;
+    if (i > 0 && v < cu[i - 1]) bad = true;
+    if (i == n && static_cast<int64_t>(v) != total) bad = true;
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0 && status != nullptr)
+    *status = SP_ERR_DEVICE_CHECK;
+}
+
+}  // namespace spb

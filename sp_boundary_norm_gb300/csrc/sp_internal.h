@@ -1,0 +1,105 @@
+// Internal declarations shared by the host entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sp_boundary.h"
+
+namespace spb {
+
+// Where each token of the (b, s) token grid lives: sequence shard k holds
+// positions [off[k], off[k+1]) of every batch row (o_k = floor(k*s/t)).
+struct ShardMap {
+  int64_t off[SP_MAX_RANKS + 1];
+  int64_t b, s, h;
+  int32_t t;
+};
+
+struct FwdParams {
+  ShardMap map;
+  const uint16_t* partials[SP_MAX_RANKS];
+  const uint16_t* residual[SP_MAX_RANKS];
+  uint16_t* z[SP_MAX_RANKS];
+  uint8_t* mask[SP_MAX_RANKS];
+  float* mean[SP_MAX_RANKS];
+  float* rstd[SP_MAX_RANKS];
+  uint16_t* gathered[SP_MAX_RANKS];
+  const uint16_t* bias;
+  const uint16_t* gamma;
+  const uint16_t* beta;
+  const int32_t* cu_seqlens;
+  int32_t n_seqs;
+  int32_t n_gather;
+  int32_t norm;          // sp_norm_t
+  uint32_t thr;          // keep iff draw >= thr; 0 disables dropout
+  float scale;           // float(1/(1-p))
+  float eps;
+  uint32_t key0, key1;   // Philox key = seed
+  uint32_t off0, off1;   // Philox counter words 2, 3 = offset
+  int64_t rows;          // b * s
+  int32_t* status;
+};
+
+struct BwdParams {
+  ShardMap map;
+  const uint16_t* dy[SP_MAX_RANKS];
+  const uint16_t* z[SP_MAX_RANKS];
+  const uint8_t* mask[SP_MAX_RANKS];
+  const float* mean[SP_MAX_RANKS];
+  const float* rstd[SP_MAX_RANKS];
+  const uint16_t* dz_skip[SP_MAX_RANKS];
+  uint16_t* dresidual[SP_MAX_RANKS];
+  uint16_t* dgathered[SP_MAX_RANKS];
+  const uint16_t* gamma;
+  const int32_t* cu_seqlens;
+  int32_t n_seqs;
+  int32_t n_gather;
+  int32_t norm;
+  int32_t has_skip;
+  float scale;
+  int64_t rows;
+  float* ws;             // [gridDim.x][3][h] per-block parameter-gradient partials
+  int32_t* status;
+};
+
+struct ParamReduceParams {
+  const float* ws;       // [nblk][3][h]
+  int32_t nblk;
+  int64_t h;
+  float* out[3];         // dgamma, dbeta, dbias (NULL = skip)
+};
+
+struct CopyParams {
+  ShardMap map;
+  const uint16_t* src[SP_MAX_RANKS];
+  uint16_t* dst[SP_MAX_RANKS];
+  int32_t n_dst;
+  const int32_t* cu_seqlens;
+  int32_t n_seqs;
+  int64_t rows;
+  int32_t* status;
+};
+
+// Launch shapes chosen on the host.
+struct LaunchShape {
+  int threads;     // threads per block (consumers of one token row)
+  int maxc;        // compile-time bound on chunks per row (1, 2, 4, 8)
+  int stages;      // cp.async pipeline depth
+  int grid;        // blocks
+  size_t smem;     // dynamic shared memory bytes
+};
+
+int device_sm_count();
+
+// Kernel entry of a (threads, chunks, stages) shape, or nullptr if that shape
+// is not instantiated.
+const void* fwd_kernel(int threads, int maxc, int stages);
+const void* bwd_kernel(int threads, int maxc, int stages);
+
+cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st);
+cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st);
+cudaError_t launch_reduce_scatter(const CopyParams& p, int t, cudaStream_t st);
+cudaError_t launch_debug_philox(const uint32_t* in, uint32_t* out, int64_t n, cudaStream_t st);
+
+}  // namespace spb

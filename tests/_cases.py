@@ -1,0 +1,175 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path, run the oracle,
+compare at the tolerances stated in ``oracle.compare``."""
+import numpy as np
+import torch
+
+from oracle import boundary as ob
+from oracle import compare
+from sp_boundary_norm_gb300 import binding as sp
+from sp_boundary_norm_gb300 import workloads as wl
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+def f32(x):
+    return None if x is None else x.float().cpu().numpy()
+
+
+def alloc_fwd(w, n_gather, dev=DEV, fill=None):
+    sizes = w.shard_sizes()
+    mk = lambda shape, dt: (torch.empty(shape, dtype=dt, device=dev) if fill is None else
+                            torch.full(shape, fill, dtype=dt, device=dev) if dt.is_floating_point
+                            else torch.full(shape, 0xAB, dtype=dt, device=dev))
+    return {
+        "z": [mk((w.b, n, w.h), torch.bfloat16) for n in sizes],
+        "mask": [mk((w.b, n, w.h), torch.uint8) for n in sizes],
+        "mean": [mk((w.b, n), torch.float32) for n in sizes] if w.norm == "layernorm" else None,
+        "rstd": [mk((w.b, n), torch.float32) for n in sizes],
+        "gathered": [mk((w.b, w.s, w.h), torch.bfloat16) for _ in range(n_gather)],
+    }
+
+
+def run_fwd(w, inp, n_gather=None, out=None, cu_seqlens=None):
+    n_gather = w.n_gather if n_gather is None else n_gather
+    out = alloc_fwd(w, n_gather) if out is None else out
+    if cu_seqlens is None and w.ragged:
+        cu_seqlens = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(DEV)
+    sp.sp_rs_norm_fwd(inp["partials"], inp["residual"], inp["bias"], inp["gamma"], inp["beta"],
+                      eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                      cu_seqlens=cu_seqlens, z_out=out["z"], mask_out=out["mask"],
+                      mean_out=out["mean"], rstd_out=out["rstd"], gathered=out["gathered"])
+    return out
+
+
+def alloc_bwd(w, n_gather, dev=DEV):
+    sizes = w.shard_sizes()
+    ws = torch.empty(max(16, sp.sp_norm_bwd_workspace_bytes(w.b, w.s, w.h, w.t, w.norm)),
+                     dtype=torch.uint8, device=dev)
+    return {
+        "dres": [torch.empty((w.b, n, w.h), dtype=torch.bfloat16, device=dev) for n in sizes],
+        "dgat": [torch.empty((w.b, w.s, w.h), dtype=torch.bfloat16, device=dev)
+                 for _ in range(n_gather)],
+        "dgamma": torch.empty(w.h, dtype=torch.float32, device=dev),
+        "dbeta": torch.empty(w.h, dtype=torch.float32, device=dev),
+        "dbias": torch.empty(w.h, dtype=torch.float32, device=dev),
+        "ws": ws,
+    }
+
+
+def run_bwd(w, fwd_out, gamma, dy, dz_skip=None, n_gather=None, out=None, cu_seqlens=None):
+    n_gather = w.n_gather if n_gather is None else n_gather
+    out = alloc_bwd(w, n_gather) if out is None else out
+    if cu_seqlens is None and w.ragged:
+        cu_seqlens = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(DEV)
+    sp.sp_norm_bwd(dy, fwd_out["z"], fwd_out["mask"], fwd_out["mean"], fwd_out["rstd"], gamma,
+                   dz_skip, s=w.s, p=w.p, norm=w.norm, cu_seqlens=cu_seqlens,
+                   dresidual=out["dres"], dgathered=out["dgat"], dgamma=out["dgamma"],
+                   dbeta=out["dbeta"] if w.norm == "layernorm" else None, dbias=out["dbias"],
+                   workspace=out["ws"])
+    return out
+
+
+def token_shard(w, g):
+    """(shard k, local row) of global token g for b == 1 or dense b > 1."""
+    bi, si = divmod(int(g), w.s)
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    k = max(j for j in range(w.t) if offs[j] <= si and offs[j + 1] > si)
+    return k, bi * (offs[k + 1] - offs[k]) + (si - offs[k])
+
+
+def sample_tokens(w, n, seed=0):
+    """Spread of tokens incl. the first and last token of every shard."""
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    picks = set()
+    for bi in range(w.b):
+        for k in range(w.t):
+            if offs[k + 1] > offs[k]:
+                picks.add(bi * w.s + offs[k])
+                picks.add(bi * w.s + offs[k + 1] - 1)
+    rng = np.random.default_rng(seed)
+    picks.update(int(x) for x in rng.integers(0, w.b * w.s, size=max(0, n - len(picks))))
+    return np.array(sorted(picks), dtype=np.int64)
+
+
+def check_fwd_rows(w, inp, out, tokens):
+    """Compare the given tokens' outputs with the oracle's per-token forward."""
+    t, h = w.t, w.h
+    toks = torch.from_numpy(tokens).to(DEV)
+    flat = [P.reshape(-1, h) for P in inp["partials"]]
+    prow = np.stack([f32(F.index_select(0, toks)) for F in flat])          # (t, n, h)
+    locs = [token_shard(w, g) for g in tokens]
+    rrow = np.stack([f32(inp["residual"][k].reshape(-1, h)[l]) for k, l in locs])
+    ref = ob.forward_rows(prow, rrow, tokens, f32(inp["bias"]), f32(inp["gamma"]),
+                          f32(inp["beta"]), eps=w.eps, p=w.p, seed=w.seed, offset=w.offset,
+                          norm=w.norm)
+    z = np.stack([compare.bf16_bits(out["z"][k].reshape(-1, h)[l]) for k, l in locs])
+    assert np.array_equal(z, compare.bf16_bits(ref["z"])), "Z must be bit-exact"
+    m = np.stack([out["mask"][k].reshape(-1, h)[l].cpu().numpy() for k, l in locs])
+    assert np.array_equal(m, ref["mask"]), "mask must be bit-exact"
+    rs = np.array([float(out["rstd"][k].reshape(-1)[l]) for k, l in locs])
+    assert not compare.f32_rel_mismatch(rs, ref["rstd"]).any(), "rstd"
+    if w.norm == "layernorm":
+        mu = np.array([float(out["mean"][k].reshape(-1)[l]) for k, l in locs])
+        assert not compare.f32_rel_mismatch(mu, ref["mean"]).any(), "mean"
+    for j, g in enumerate(out["gathered"]):
+        o = compare.bf16_bits(g.reshape(-1, h).index_select(0, toks))
+        bad = compare.bf16_mismatch(o, ref["out_exact"], ref["out_magnitude"])
+        assert not bad.any(), f"gathered[{j}]: {bad.sum()} elements off"
+    return ref
+
+
+def check_bwd_rows(w, fwd_out, gamma, dy, dz_skip, out, tokens):
+    h = w.h
+    locs = [token_shard(w, g) for g in tokens]
+    pick = lambda lst, k, l: lst[k].reshape(-1, h)[l]
+    dyr = np.stack([f32(pick(dy, k, l)) for k, l in locs])
+    zr = np.stack([f32(pick(fwd_out["z"], k, l)) for k, l in locs])
+    mr = np.stack([pick(fwd_out["mask"], k, l).cpu().numpy() for k, l in locs])
+    rs = np.array([float(fwd_out["rstd"][k].reshape(-1)[l]) for k, l in locs])
+    mu = (np.array([float(fwd_out["mean"][k].reshape(-1)[l]) for k, l in locs])
+          if w.norm == "layernorm" else None)
+    sk = None if dz_skip is None else np.stack([f32(pick(dz_skip, k, l)) for k, l in locs])
+    ref = ob.backward_rows(dyr, zr, mr, mu, rs, f32(gamma), sk, p=w.p, norm=w.norm)
+    dres = np.stack([compare.bf16_bits(pick(out["dres"], k, l)) for k, l in locs])
+    bad = compare.bf16_mismatch(dres, ref["dz"], ref["dz_magnitude"])
+    assert not bad.any(), f"dresidual: {bad.sum()} elements off"
+    toks = torch.from_numpy(tokens).to(DEV)
+    scale = float(ob.dropout_scale(w.p))
+    for j, g in enumerate(out["dgat"]):
+        o = compare.bf16_bits(g.reshape(-1, h).index_select(0, toks))
+        bad = compare.bf16_mismatch(o, ref["dypre_exact"], ref["dz_magnitude"] * scale)
+        assert not bad.any(), f"dgathered[{j}]: {bad.sum()} elements off"
+    return ref
+
+
+def check_param_grads(w, fwd_out, gamma, dy, dz_skip, out):
+    """Full oracle parameter gradients, shard by shard (float64)."""
+    h = w.h
+    acc = {n: np.zeros(h) for n in ("dgamma", "dbeta", "dbias")}
+    sq = {n: np.zeros(h) for n in acc}
+    g = f32(gamma)
+    for k in range(w.t):
+        n = fwd_out["z"][k].numel() // h
+        if n == 0:
+            continue
+        step = 4096
+        for lo in range(0, n, step):
+            sl = slice(lo, min(n, lo + step))
+            rows = lambda x: None if x is None else f32(x[k].reshape(-1, h)[sl])
+            one = ob.backward_rows(
+                rows(dy), rows(fwd_out["z"]), fwd_out["mask"][k].reshape(-1, h)[sl].cpu().numpy(),
+                None if w.norm != "layernorm" else fwd_out["mean"][k].reshape(-1)[sl].cpu().numpy(),
+                fwd_out["rstd"][k].reshape(-1)[sl].cpu().numpy(), g, rows(dz_skip), p=w.p,
+                norm=w.norm)
+            for name in acc:
+                terms = one[name + "_terms"]
+                if terms is None:
+                    continue
+                acc[name] += terms.sum(axis=0)
+                sq[name] += (terms * terms).sum(axis=0)
+    names = ["dgamma", "dbias"] + (["dbeta"] if w.norm == "layernorm" else [])
+    for name in names:
+        got = out[name].cpu().numpy()
+        bad = compare.colsum_mismatch(got, acc[name], np.sqrt(sq[name]))
+        assert not bad.any(), f"{name}: {bad.sum()} channels off, max err " \
+            f"{np.max(np.abs(got - acc[name])):.3g}"

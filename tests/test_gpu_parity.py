@@ -1,0 +1,360 @@
+"""GPU parity: the CUDA boundary (through the C ABI) against the CPU oracle.
+
+Bit-exact: shard indexing, gathered layout, Z (pinned float32 order), the
+dropout mask.  Tolerances (``oracle.compare``): bf16 outputs within 1 ulp (or
+float32-accuracy floor on cancellation), float32 stats 1e-5 relative,
+parameter-gradient sums 1e-5 of their terms' root-sum-square.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import boundary as ob
+from oracle import compare
+from sp_boundary_norm_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("_cases")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+
+
+def _full_fwd_compare(w, inp, out):
+    ref = ob.rs_norm_fwd([C.f32(x) for x in inp["partials"]], [C.f32(x) for x in inp["residual"]],
+                         C.f32(inp["bias"]), C.f32(inp["gamma"]), C.f32(inp["beta"]), eps=w.eps,
+                         p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                         n_gather=len(out["gathered"]))
+    for k in range(w.t):
+        assert np.array_equal(compare.bf16_bits(out["z"][k]), compare.bf16_bits(ref["z"][k])), k
+        assert np.array_equal(out["mask"][k].cpu().numpy(), ref["mask"][k]), k
+        assert not compare.f32_rel_mismatch(out["rstd"][k].cpu().numpy(), ref["rstd"][k]).any()
+        if w.norm == "layernorm":
+            assert not compare.f32_rel_mismatch(out["mean"][k].cpu().numpy(), ref["mean"][k]).any()
+    out_exact = np.concatenate(ref["out_exact"], axis=1)
+    mag = np.concatenate([ob._norm_rows(z.reshape(-1, w.h).astype(np.float64), C.f32(inp["gamma"]),
+                                        C.f32(inp["beta"]), w.eps, w.norm)[3].reshape(z.shape)
+                          for z in ref["z"]], axis=1)
+    for j, g in enumerate(out["gathered"]):
+        bad = compare.bf16_mismatch(compare.bf16_bits(g), out_exact, mag)
+        assert not bad.any(), f"gathered[{j}]: {bad.sum()} off"
+    return ref
+
+
+@pytest.mark.parametrize("name", ["tiny", "trace4k"])
+def test_forward_full_compare(name):
+    w = wl.WORKLOADS[name]
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    _full_fwd_compare(w, inp, out)
+
+
+@pytest.mark.parametrize("variant", [
+    dict(norm="rmsnorm", eps=1e-6),
+    dict(p=0.0),
+    dict(t=1),
+    dict(t=1, p=0.0),
+    dict(t=3, s=48),
+    dict(t=16, s=64),
+    dict(b=3, s=40, t=4),
+    dict(h=8, s=16),
+    dict(h=24, s=16),
+    dict(h=520, s=32),
+    dict(h=2056, s=16),
+    dict(h=5120, s=32),
+    dict(h=16384, s=8),
+    dict(n_gather=2),
+    dict(n_gather=0),
+    dict(seed=2**40 + 17, offset=2**33 + 5),
+    dict(p=0.9),
+])
+def test_forward_variants_full_compare(variant):
+    base = wl.Workload("v", t=2, b=1, s=64, h=512, draw_seed=21)
+    w = base.with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    _full_fwd_compare(w, inp, out)
+
+
+def test_forward_gathered_copies_identical_and_layout():
+    w = wl.Workload("g", t=4, b=2, s=32, h=256, n_gather=4, draw_seed=22)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    g0 = out["gathered"][0]
+    for g in out["gathered"][1:]:
+        assert torch.equal(g.view(torch.int16), g0.view(torch.int16))
+
+
+@pytest.mark.parametrize("lengths,t", [((5, 17, 3, 40), 8), ((3,), 8), ((100, 1, 1), 3),
+                                       ((33, 64, 7, 1, 90, 12), 5)])
+def test_forward_ragged_packed_full_compare(lengths, t):
+    w = wl.Workload("r", t=t, b=1, s=sum(lengths), h=512, seqlens=tuple(lengths), draw_seed=23)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    _full_fwd_compare(w, inp, out)
+
+
+def test_forward_ragged_workload_sampled():
+    w = wl.WORKLOADS["ragged"]
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.check_fwd_rows(w, inp, out, C.sample_tokens(w, 160))
+
+
+def test_forward_70b_sampled_and_properties():
+    w = wl.WORKLOADS["70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.check_fwd_rows(w, inp, out, C.sample_tokens(w, 96))
+    # properties over the whole output: drop rate, finiteness, gathered == shards
+    kept = sum(int(m.sum()) for m in out["mask"])
+    n = w.tokens * w.h
+    assert abs((1 - kept / n) - w.p) < 5 * np.sqrt(w.p * (1 - w.p) / n)
+    g = out["gathered"][0]
+    assert torch.isfinite(g.float()).all()
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    for k in range(w.t):
+        blk = g[:, offs[k]:offs[k + 1], :].float()
+        assert torch.isfinite(out["z"][k].float()).all()
+        # LayerNorm output rows: mean ~ beta mean, finite stats
+        assert torch.isfinite(out["rstd"][k]).all() and torch.isfinite(out["mean"][k]).all()
+        assert blk.shape[1] == w.shard_sizes()[k]
+
+
+def test_forward_empty_and_tiny_sequences():
+    w = wl.Workload("e", t=4, b=1, s=0, h=64)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    assert all(z.numel() == 0 for z in out["z"])
+
+
+def test_forward_mask_independent_of_t_on_gpu():
+    masks = []
+    for t in (1, 2, 8):
+        w = wl.Workload("m", t=t, b=1, s=64, h=256, draw_seed=24)
+        inp = wl.forward_inputs(w, C.DEV)
+        out = C.run_fwd(w, inp)
+        masks.append(torch.cat(out["mask"], dim=1))
+    assert torch.equal(masks[0], masks[1]) and torch.equal(masks[0], masks[2])
+
+
+def test_forward_deterministic_and_writes_only_its_outputs():
+    w = wl.Workload("d", t=4, b=1, s=128, h=1024, n_gather=2, draw_seed=25)
+    inp = wl.forward_inputs(w, C.DEV)
+    # outputs poisoned first: every element must be overwritten
+    out1 = C.run_fwd(w, inp, out=C.alloc_fwd(w, 2, fill=float("nan")))
+    out2 = C.run_fwd(w, inp, out=C.alloc_fwd(w, 2, fill=-7.0))
+    torch.cuda.synchronize()
+    for key in ("z", "gathered"):
+        for a, b in zip(out1[key], out2[key]):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for key in ("mask", "mean", "rstd"):
+        for a, b in zip(out1[key], out2[key]):
+            assert torch.equal(a, b)
+
+
+def test_guard_bands_untouched():
+    """Outputs carved from larger buffers: bytes around them keep their pattern."""
+    w = wl.Workload("gb", t=2, b=1, s=96, h=264, n_gather=1, draw_seed=26)
+    inp = wl.forward_inputs(w, C.DEV)
+    pad = 4096
+    sizes = w.shard_sizes()
+
+    def carve(shape, dtype):
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        raw = torch.full((n + 2 * pad,), 0x5A, dtype=torch.uint8, device=C.DEV)
+        return raw, raw[pad:pad + n].view(dtype).view(shape)
+
+    bufs, out = [], {"z": [], "mask": [], "mean": [], "rstd": [], "gathered": []}
+    for n in sizes:
+        for key, shape, dt in (("z", (1, n, w.h), torch.bfloat16), ("mask", (1, n, w.h), torch.uint8),
+                               ("mean", (1, n), torch.float32), ("rstd", (1, n), torch.float32)):
+            raw, v = carve(shape, dt)
+            bufs.append(raw)
+            out[key].append(v)
+    raw, v = carve((1, w.s, w.h), torch.bfloat16)
+    bufs.append(raw)
+    out["gathered"].append(v)
+    C.run_fwd(w, inp, out=out)
+    torch.cuda.synchronize()
+    for raw in bufs:
+        assert bool((raw[:pad] == 0x5A).all()) and bool((raw[-pad:] == 0x5A).all())
+
+
+def test_invalid_cu_seqlens_flagged_on_device():
+    w = wl.Workload("bad", t=2, b=1, s=20, h=64, seqlens=(10, 10), draw_seed=27)
+    inp = wl.forward_inputs(w, C.DEV)
+    bad = torch.tensor([0, 10, 19], dtype=torch.int32, device=C.DEV)   # ends at 19 != 20
+    C.run_fwd(w, inp, cu_seqlens=bad)
+    torch.cuda.synchronize()
+    with pytest.raises(C.sp.SpError) as e:
+        C.sp.check_device_status(C.DEV)
+    assert e.value.name == "SP_ERR_DEVICE_CHECK"
+    C.run_fwd(w, inp)                                                    # a good call after
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+
+
+def test_injected_failure_launches_nothing():
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.alloc_fwd(w, 1, fill=3.0)
+    C.sp.sp_debug_inject(4)
+    with pytest.raises(C.sp.SpError) as e:
+        C.run_fwd(w, inp, out=out)
+    assert e.value.name == "SP_ERR_CUDA"
+    torch.cuda.synchronize()
+    assert bool((out["gathered"][0].float() == 3.0).all())
+    C.run_fwd(w, inp, out=out)                                           # hook disarmed
+
+
+# ------------------------------------------------------------------ backward
+
+def _bwd_setup(w, with_skip=False, n_gather=1):
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    b = wl.backward_inputs(w, C.DEV, with_skip=with_skip)
+    out = C.run_bwd(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], n_gather=n_gather)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    return inp, fwd, b, out
+
+
+@pytest.mark.parametrize("variant", [
+    dict(),
+    dict(norm="rmsnorm", eps=1e-6),
+    dict(p=0.0),
+    dict(t=1),
+    dict(t=3, s=48),
+    dict(b=2, s=40, t=4),
+    dict(h=8, s=16),
+    dict(h=520, s=32),
+    dict(h=5120, s=24),
+    dict(h=16384, s=8),
+    dict(n_gather=3),
+    dict(n_gather=0),
+])
+@pytest.mark.parametrize("with_skip", [False, True])
+def test_backward_full_compare(variant, with_skip):
+    base = wl.Workload("b", t=2, b=1, s=64, h=512, draw_seed=31)
+    w = base.with_(**variant)
+    inp, fwd, b, out = _bwd_setup(w, with_skip, n_gather=w.n_gather)
+    toks = np.arange(w.tokens, dtype=np.int64)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out, toks)
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out)
+
+
+def test_backward_ragged_packed():
+    lengths = (5, 17, 3, 40, 1, 9)
+    w = wl.Workload("rb", t=4, b=1, s=sum(lengths), h=256, seqlens=lengths, draw_seed=32)
+    inp, fwd, b, out = _bwd_setup(w)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], None, out, np.arange(w.tokens))
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
+
+
+@pytest.mark.parametrize("name", ["bwd70b", "bwd70b_rms"])
+def test_backward_70b_sampled_and_param_grads(name):
+    w = wl.WORKLOADS[name]
+    inp, fwd, b, out = _bwd_setup(w)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], None, out, C.sample_tokens(w, 64))
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
+
+
+def test_backward_deterministic():
+    w = wl.Workload("det", t=4, b=1, s=512, h=2048, draw_seed=33)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    o1 = C.run_bwd(w, fwd, inp["gamma"], dy)
+    o2 = C.run_bwd(w, fwd, inp["gamma"], dy)
+    torch.cuda.synchronize()
+    for key in ("dgamma", "dbeta", "dbias"):
+        assert torch.equal(o1[key], o2[key]), key
+    for a, c in zip(o1["dres"], o2["dres"]):
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_backward_empty_gives_zero_param_grads():
+    w = wl.Workload("e", t=2, b=1, s=0, h=64)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    out = C.alloc_bwd(w, 1)
+    for key in ("dgamma", "dbeta", "dbias"):
+        out[key].fill_(5.0)
+    C.run_bwd(w, fwd, inp["gamma"], dy, out=out)
+    torch.cuda.synchronize()
+    for key in ("dgamma", "dbeta", "dbias"):
+        assert bool((out[key] == 0).all())
+
+
+# --------------------------------------------------------- collectives alone
+
+@pytest.mark.parametrize("t,b,s,h,n_gather", [(2, 1, 64, 512, 1), (8, 1, 256, 1024, 8),
+                                              (3, 2, 33 * 3, 40, 2), (4, 1, 4096, 4096, 1)])
+def test_allgather_and_reduce_scatter_bit_exact(t, b, s, h, n_gather):
+    from oracle import collectives as coll
+    w = wl.Workload("c", t=t, b=b, s=s, h=h, draw_seed=41)
+    inp = wl.forward_inputs(w, C.DEV)
+    sizes = w.shard_sizes()
+    shards = [torch.empty((b, n, h), dtype=torch.bfloat16, device=C.DEV) for n in sizes]
+    C.sp.sp_reduce_scatter_seq(inp["partials"], shards)
+    gathered = [torch.empty((b, s, h), dtype=torch.bfloat16, device=C.DEV) for _ in range(n_gather)]
+    C.sp.sp_allgather_seq(shards, gathered, s=s)
+    torch.cuda.synchronize()
+    ref_shards, _ = coll.reduce_scatter_seq([C.f32(x) for x in inp["partials"]])
+    from oracle.bf16 import bf16_round
+    for k in range(t):
+        assert np.array_equal(compare.bf16_bits(shards[k]),
+                              compare.bf16_bits(bf16_round(ref_shards[k])))
+    full = np.concatenate([bf16_round(x) for x in ref_shards], axis=1)
+    for g in gathered:
+        assert np.array_equal(compare.bf16_bits(g), compare.bf16_bits(full))
+
+
+def test_fused_gather_equals_unfused_gather_of_shards():
+    """g fused into the norm kernel == g applied afterwards to the shards' O."""
+    w = wl.Workload("fu", t=4, b=1, s=256, h=1024, n_gather=1, draw_seed=42)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp, n_gather=1)
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    o_shards = [out["gathered"][0][:, offs[k]:offs[k + 1], :].contiguous() for k in range(w.t)]
+    g2 = [torch.empty_like(out["gathered"][0])]
+    C.sp.sp_allgather_seq(o_shards, g2, s=w.s)
+    torch.cuda.synchronize()
+    assert torch.equal(g2[0].view(torch.int16), out["gathered"][0].view(torch.int16))
+
+
+def test_device_philox_matches_oracle():
+    from oracle import philox
+    rng = np.random.default_rng(3)
+    n = 4096
+    words = rng.integers(0, 2**32, size=(n, 6), dtype=np.uint64).astype(np.uint32)
+    words[0] = 0
+    words[1] = 0xFFFFFFFF
+    dev_out = C.sp.sp_debug_philox(torch.from_numpy(words.view(np.int32)).to(C.DEV))
+    got = dev_out.cpu().numpy().view(np.uint32)
+    for i in range(0, n, 97):
+        ref = philox.philox4x32([np.array([words[i, j]]) for j in range(4)],
+                                (int(words[i, 4]), int(words[i, 5])))
+        assert [int(r[0]) for r in ref] == list(got[i])
+    ref = philox.philox4x32([words[:, j] for j in range(4)], (0, 0))   # vectorised key 0 rows
+    zero_key = (words[:, 4] == 0) & (words[:, 5] == 0)
+    for j in range(4):
+        assert np.array_equal(got[zero_key, j], ref[j][zero_key])
