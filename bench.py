@@ -334,6 +334,8 @@ def run_ours(args):
         _build.build_library()
     barrier(world, device)
     w = wl.WORKLOADS[args.workload]
+    if args.s:
+        w = w.with_(s=args.s, name=f"{w.name}-s{args.s}")
     step = Step(w, device, n_gather=args.n_gather)
     total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world, device)
     rejected = False
@@ -457,6 +459,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="70b", choices=["70b", "trace4k", "ragged", "tiny"])
+    ap.add_argument("--s", type=int, default=0,
+                    help="override the sequence length (smaller cases for profiling)")
     ap.add_argument("--n-gather", type=int, default=1)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
