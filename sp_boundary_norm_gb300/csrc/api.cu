@@ -137,54 +137,42 @@ constexpr size_t kSmemPerSm = 228 * 1024;     // sm_100-class shared memory per 
 constexpr size_t kSmemPerBlock = 227 * 1024;  // opt-in maximum per block
 constexpr size_t kReserve = 1024;             // per-block reservation
 
-// (threads, chunks) for a row of h channels: every thread owns 8 channels of
-// each chunk of 8*threads channels.
-void row_shape(int64_t h, int* threads, int* maxc) {
-  const int64_t nvec = h / 8;
-  if (nvec <= 64) {
-    *threads = 64;
-    *maxc = 1;
-  } else {
-    *threads = 256;
-    *maxc = pow2_at_least(static_cast<int>((nvec + 255) / 256));
-  }
-}
-
-// Pick (stages, blocks per SM) with the largest per-SM pipeline depth that
-// fits in shared memory, then cap the grid at what is resident.
-LaunchShape pick_shape(const void* (*kernel)(int, int, int), int which, int64_t rows, int64_t h,
-                       size_t stage_bytes, size_t red_bytes, const int* stage_opts, int n_opts,
-                       int default_stages, int default_blocks) {
+// Choose the pipeline depth (`stages`: chunks for the forward, rows for the
+// backward) and blocks per SM: start from the requested pair and shrink, blocks
+// first, until the shared memory fits; then cap the grid at what the
+// occupancy calculator says is resident (persistent kernels: no block waits
+// for another, so a larger grid would only queue).
+template <typename KernelOf>
+LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t unit_bytes,
+                       size_t fixed_bytes, const int* opts, int n_opts, int want_stages,
+                       int want_blocks, KernelOf kernel_of) {
   LaunchShape ls{};
-  row_shape(h, &ls.threads, &ls.maxc);
+  ls.threads = threads;
+  ls.maxc = maxc;
   int stages = g_tune[which][0].load();
   int bps = g_tune[which][1].load();
-  if (stages == 0) stages = default_stages;
-  if (bps == 0) bps = default_blocks;
-  // shrink until it fits
+  if (stages == 0) stages = want_stages;
+  if (bps == 0) bps = want_blocks;
   auto fits = [&](int st, int bp) {
-    const size_t per_block = st * stage_bytes + red_bytes;
+    const size_t per_block = st * unit_bytes + fixed_bytes;
     return per_block <= kSmemPerBlock && bp * (per_block + kReserve) <= kSmemPerSm;
   };
   bool ok = false;
   for (int bp = bps; bp >= 1 && !ok; --bp) {
     for (int i = 0; i < n_opts && !ok; ++i) {
-      const int st = stage_opts[i];
-      if (st > stages) continue;
-      if (fits(st, bp)) {
-        stages = st;
-        bps = bp;
-        ok = true;
-      }
+      if (opts[i] > stages || !fits(opts[i], bp)) continue;
+      stages = opts[i];
+      bps = bp;
+      ok = true;
     }
   }
   if (!ok) {
-    stages = stage_opts[n_opts - 1];
+    stages = opts[n_opts - 1];
     bps = 1;
   }
   ls.stages = stages;
-  ls.smem = stages * stage_bytes + red_bytes;
-  const void* fn = kernel(ls.threads, ls.maxc, ls.stages);
+  ls.smem = stages * unit_bytes + fixed_bytes;
+  const void* fn = kernel_of(stages);
   int occ = bps;
   if (fn != nullptr &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem) ==
@@ -202,23 +190,41 @@ LaunchShape pick_shape(const void* (*kernel)(int, int, int), int which, int64_t 
   return ls;
 }
 
-const int kFwdStages[] = {6, 4, 3, 2};
-const int kBwdStages[] = {8, 4, 2};
+const int kFwdStages[] = {4, 3, 2};
+const int kBwdRing[] = {4, 3, 2};
 
+// Forward: every thread owns 8 channels of each chunk of 8 * threads channels;
+// one pipeline stage holds the chunk of the t partials and the residual, and
+// the row's Z waits in shared memory for the statistics.
 LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
-  int threads, maxc;
-  row_shape(h, &threads, &maxc);
+  const int threads = (h / 8 <= 64) ? 64 : 256;
+  const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
-  return pick_shape(fwd_kernel, 0, rows, h, stage, 2 * 32 * sizeof(float), kFwdStages, 4,
-                    /*stages=*/6, /*blocks per SM=*/1);
+  const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float);
+  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 3,
+                    /*stages=*/3, /*blocks per SM=*/threads == 64 ? 4 : 2,
+                    [&](int st) { return fwd_kernel(threads, t, st); });
 }
 
+// Backward: a ring of whole rows (dY, Z, mask, optional skip gradient).
 LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip) {
+  const int64_t nvec = h / 8;
   int threads, maxc;
-  row_shape(h, &threads, &maxc);
-  const size_t stage = static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + threads * 8;
-  return pick_shape(bwd_kernel, 1, rows, h, stage, 2 * 32 * sizeof(float2), kBwdStages, 3,
-                    /*stages=*/8, /*blocks per SM=*/1);
+  if (nvec <= 64) {
+    threads = 64;
+    maxc = 1;
+  } else if (nvec <= 256) {
+    threads = 256;
+    maxc = 1;
+  } else {
+    threads = 512;
+    maxc = pow2_at_least(static_cast<int>((nvec + 511) / 512));
+  }
+  const size_t item = static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + threads * 8;
+  const size_t ring_row = item * maxc;
+  return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 3,
+                    /*ring=*/3, /*blocks per SM=*/threads == 512 ? 1 : 2,
+                    [&](int st) { return bwd_kernel(threads, maxc, st); });
 }
 
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
@@ -342,7 +348,7 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   P.status = dev_status;
 
   const LaunchShape ls = fwd_shape(rows, h, t);
-  const cudaError_t e = launch(fwd_kernel(ls.threads, ls.maxc, ls.stages), ls, &P,
+  const cudaError_t e = launch(fwd_kernel(ls.threads, t, ls.stages), ls, &P,
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_fwd launch");
   return SP_OK;

@@ -9,10 +9,12 @@
 //
 // Work layout mirrors the forward: a persistent grid, one token row per block
 // iteration, chunks of 8*T channels with thread i owning channels
-// [8i, 8i+8) of each chunk, and a per-thread cp.async pipeline that stages
-// dY, Z, the mask (and the optional skip-path gradient) of the next chunks.
-// A row needs two reductions over h (mean(dxh), mean(dxh * x_hat)); they are
-// done together, so one block barrier per row.  Because a thread owns the same
+// [8i, 8i+8) of each chunk.  Each thread stages its own pieces of dY, Z, the
+// mask (and the optional skip-path gradient) of whole rows with cp.async into
+// a ring of RING rows in shared memory, RING - 1 rows ahead; the two passes a
+// row needs (the row sums mean(dxh) and mean(dxh * x_hat), then the
+// gradients) both read the row from there.  The two sums are reduced
+// together: one block barrier per row.  Because a thread owns the same
 // channels in every row, it accumulates its channels' parameter-gradient
 // terms in registers across all rows of its block and writes one float32
 // partial per block and channel at the end; a second kernel sums the
@@ -22,22 +24,20 @@
 
 namespace spb {
 
-template <int NTHR, int MAXC, int STAGES>
+template <int NTHR, int MAXC, int RING>
 __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
-  constexpr int nthr = NTHR;
   const int64_t h = P.map.h;
-  const int64_t chunk_ch = 8LL * nthr;
-  const int nchunk = static_cast<int>((h + chunk_ch - 1) / chunk_ch);
+  constexpr int64_t kChunk = 8LL * NTHR;
+  const int nchunk = static_cast<int>((h + kChunk - 1) / kChunk);
   const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
   const bool has_skip = P.has_skip != 0;
-  const size_t v16 = static_cast<size_t>(nthr) * 16;
-  const size_t off_z = v16;
-  const size_t off_skip = 2 * v16;
+  // one staged chunk ("item"): [dY | Z | skip (optional) | mask] of all threads
+  constexpr size_t v16 = static_cast<size_t>(NTHR) * 16;
   const size_t off_mask = (has_skip ? 3 : 2) * v16;
-  const size_t stage_bytes = off_mask + static_cast<size_t>(nthr) * 8;
-  float2* red = reinterpret_cast<float2*>(smem + STAGES * stage_bytes);   // [2][32]
+  const size_t item_bytes = off_mask + static_cast<size_t>(NTHR) * 8;
+  float2* red = reinterpret_cast<float2*>(smem + RING * MAXC * item_bytes);   // [2][32]
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
@@ -48,37 +48,35 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   uint4 gam[MAXC];
 #pragma unroll
   for (int ch = 0; ch < MAXC; ++ch) {
-    const int64_t c = ch * chunk_ch + tid * 8;
+    const int64_t c = ch * kChunk + tid * 8;
     gam[ch] = (ch < nchunk && c < h) ? ldg16(P.gamma + c) : make_uint4(0, 0, 0, 0);
   }
 
-  int64_t pf_ri = 0;
-  int pf_chunk = 0, pf_stage = 0, pf_k = 0;
-  int64_t pf_local = 0;
-  if (nrows > 0) locate(P.map, blockIdx.x, pf_k, pf_local);
-
-  auto issue_next = [&]() {
-    if (pf_ri < nrows) {
-      const int64_t c = pf_chunk * chunk_ch + tid * 8;
-      if (c < h) {
-        uint8_t* slot = smem + pf_stage * stage_bytes;
-        const int64_t lo = pf_local * h + c;
-        cp_async16(slot + tid * 16, P.dy[pf_k] + lo);
-        cp_async16(slot + off_z + tid * 16, P.z[pf_k] + lo);
-        if (has_skip) cp_async16(slot + off_skip + tid * 16, P.dz_skip[pf_k] + lo);
-        cp_async8(slot + off_mask + tid * 8, P.mask[pf_k] + lo);
-      }
-      if (++pf_chunk == nchunk) {
-        pf_chunk = 0;
-        if (++pf_ri < nrows) locate(P.map, blockIdx.x + pf_ri * G, pf_k, pf_local);
+  // Stage row ri (all of its chunks, one cp.async group) into ring slot ri % RING.
+  auto issue_row = [&](int64_t ri) {
+    if (ri < nrows) {
+      int k;
+      int64_t local;
+      locate(P.map, blockIdx.x + ri * G, k, local);
+      uint8_t* base = smem + static_cast<size_t>(ri % RING) * MAXC * item_bytes;
+#pragma unroll
+      for (int ch = 0; ch < MAXC; ++ch) {
+        const int64_t c = ch * kChunk + tid * 8;
+        if (ch < nchunk && c < h) {
+          uint8_t* it = base + ch * item_bytes;
+          const int64_t lo = local * h + c;
+          cp_async16(it + tid * 16, P.dy[k] + lo);
+          cp_async16(it + v16 + tid * 16, P.z[k] + lo);
+          if (has_skip) cp_async16(it + 2 * v16 + tid * 16, P.dz_skip[k] + lo);
+          cp_async8(it + off_mask + tid * 8, P.mask[k] + lo);
+        }
       }
     }
     cp_async_commit();
-    pf_stage = (pf_stage + 1 == STAGES) ? 0 : pf_stage + 1;
   };
 
 #pragma unroll
-  for (int i = 0; i < STAGES - 1; ++i) issue_next();
+  for (int i = 0; i < RING - 1; ++i) issue_row(i);
 
   float acc_g[MAXC][8], acc_b[MAXC][8], acc_bias[MAXC][8];
 #pragma unroll
@@ -96,8 +94,8 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
     if (is_ln) cur_mean = P.mean[k0][l0];
   }
 
-  int stage = 0;
   int slot_sel = 0;
+  const float fh = static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
     const int64_t row = blockIdx.x + ri * G;
     int k;
@@ -113,63 +111,62 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
     }
     const float mean = cur_mean, rstd = cur_rstd;
 
-    uint4 dyv[MAXC], zv[MAXC], skv[MAXC];
-    uint2 mkv[MAXC];
+    issue_row(ri + RING - 1);      // refills the slot row ri - 1 used
+    cp_async_wait<RING - 1>();      // row ri has landed
+    const uint8_t* base = smem + static_cast<size_t>(ri % RING) * MAXC * item_bytes;
+
+    // ---- pass 1: the two row sums, and dgamma / dbeta terms --------------
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
-      dyv[ch] = zv[ch] = skv[ch] = make_uint4(0, 0, 0, 0);
-      mkv[ch] = make_uint2(0, 0);
-      if (ch < nchunk) {
-        issue_next();
-        cp_async_wait<STAGES - 1>();
-        const int64_t c = ch * chunk_ch + tid * 8;
-        if (c < h) {
-          const uint8_t* slot = smem + stage * stage_bytes;
-          dyv[ch] = lds16(slot + tid * 16);
-          zv[ch] = lds16(slot + off_z + tid * 16);
-          if (has_skip) skv[ch] = lds16(slot + off_skip + tid * 16);
-          mkv[ch] = lds8(slot + off_mask + tid * 8);
-          float dy[8], zf[8], g[8];
-          unpack8(dyv[ch], dy);
-          unpack8(zv[ch], zf);
-          unpack8(gam[ch], g);
+      const int64_t c = ch * kChunk + tid * 8;
+      if (ch < nchunk && c < h) {
+        const uint8_t* it = base + ch * item_bytes;
+        float dy[8], zf[8], g[8];
+        unpack8(lds16(it + tid * 16), dy);
+        unpack8(lds16(it + v16 + tid * 16), zf);
+        unpack8(gam[ch], g);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float xh = is_ln ? (zf[e] - mean) * rstd : zf[e] * rstd;
-            const float dxh = dy[e] * g[e];
-            s1 += dxh;
-            s2 += dxh * xh;
-            acc_g[ch][e] += dy[e] * xh;
-            acc_b[ch][e] += dy[e];
-          }
+        for (int e = 0; e < 8; ++e) {
+          const float xh = is_ln ? (zf[e] - mean) * rstd : zf[e] * rstd;
+          const float dxh = dy[e] * g[e];
+          s1 += dxh;
+          s2 += dxh * xh;
+          acc_g[ch][e] += dy[e] * xh;
+          acc_b[ch][e] += dy[e];
         }
-        stage = (stage + 1 == STAGES) ? 0 : stage + 1;
       }
     }
 
     const float2 s = block_sum2(s1, s2, red + 32 * slot_sel);
     slot_sel ^= 1;
-    const float fh = static_cast<float>(h);
     const float m1 = is_ln ? s.x / fh : 0.f;
     const float m2 = s.y / fh;
 
+    // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
-      const int64_t c = ch * chunk_ch + tid * 8;
+      const int64_t c = ch * kChunk + tid * 8;
       if (ch < nchunk && c < h) {
+        const uint8_t* it = base + ch * item_bytes;
         float dy[8], zf[8], g[8], sk[8], dz[8], dp[8];
-        unpack8(dyv[ch], dy);
-        unpack8(zv[ch], zf);
+        unpack8(lds16(it + tid * 16), dy);
+        unpack8(lds16(it + v16 + tid * 16), zf);
         unpack8(gam[ch], g);
-        unpack8(skv[ch], sk);   // zeros when there is no skip gradient
-        const uint32_t keep = bytes8_to_bits(mkv[ch]);
+        if (has_skip) {
+          unpack8(lds16(it + 2 * v16 + tid * 16), sk);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sk[e] = 0.f;
+        }
+        const uint2 mk = lds8(it + off_mask + tid * 8);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float xh = is_ln ? (zf[e] - mean) * rstd : zf[e] * rstd;
           const float dxh = dy[e] * g[e];
           dz[e] = rstd * (dxh - m1 - xh * m2) + sk[e];
-          dp[e] = ((keep >> e) & 1u) ? dz[e] * P.scale : 0.f;
+          const uint32_t kb = ((e < 4 ? mk.x : mk.y) >> (8 * (e & 3))) & 0xFFu;
+          dp[e] = kb ? dz[e] * P.scale : 0.f;
           acc_bias[ch][e] += dp[e];
         }
         st16_stream(P.dresidual[k] + local * h + c, pack8(dz));
@@ -186,7 +183,7 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   float* wsb = P.ws + static_cast<int64_t>(blockIdx.x) * 3 * h;
 #pragma unroll
   for (int ch = 0; ch < MAXC; ++ch) {
-    const int64_t c = ch * chunk_ch + tid * 8;
+    const int64_t c = ch * kChunk + tid * 8;
     if (ch < nchunk && c < h) {
       float4* dg = reinterpret_cast<float4*>(wsb + c);
       float4* db = reinterpret_cast<float4*>(wsb + h + c);
@@ -215,25 +212,25 @@ __global__ void __launch_bounds__(256) param_reduce_kernel(const ParamReducePara
 }
 
 template <int NTHR, int MAXC>
-static const void* bwd_kernel_s(int stages) {
-  switch (stages) {
+static const void* bwd_kernel_s(int ring) {
+  switch (ring) {
     case 2: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 2>);
+    case 3: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 3>);
     case 4: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 4>);
-    case 8: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 8>);
     default: return nullptr;
   }
 }
 
-// Instantiated shapes: (threads, chunks) = (64, 1) for h <= 512, else
-// (256, 1 | 2 | 4 | 8); pipeline depth 2, 4 or 8.
-const void* bwd_kernel(int threads, int maxc, int stages) {
-  if (threads == 64) return maxc == 1 ? bwd_kernel_s<64, 1>(stages) : nullptr;
-  if (threads != 256) return nullptr;
+// Instantiated shapes (threads, chunks per row): (64, 1) for h <= 512,
+// (256, 1) for h <= 2048, (512, 1 | 2 | 4) above; ring of 2, 3 or 4 rows.
+const void* bwd_kernel(int threads, int maxc, int ring) {
+  if (threads == 64) return maxc == 1 ? bwd_kernel_s<64, 1>(ring) : nullptr;
+  if (threads == 256) return maxc == 1 ? bwd_kernel_s<256, 1>(ring) : nullptr;
+  if (threads != 512) return nullptr;
   switch (maxc) {
-    case 1: return bwd_kernel_s<256, 1>(stages);
-    case 2: return bwd_kernel_s<256, 2>(stages);
-    case 4: return bwd_kernel_s<256, 4>(stages);
-    case 8: return bwd_kernel_s<256, 8>(stages);
+    case 1: return bwd_kernel_s<512, 1>(ring);
+    case 2: return bwd_kernel_s<512, 2>(ring);
+    case 4: return bwd_kernel_s<512, 4>(ring);
     default: return nullptr;
   }
 }

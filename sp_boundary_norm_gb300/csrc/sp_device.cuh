@@ -70,6 +70,25 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
+// Keep flags (0/1) of 4 draws against thr, and their 4 mask bytes.
+__device__ __forceinline__ uint32_t keep_bytes4(uint4 u, uint32_t thr) {
+  const uint32_t k0 = u.x >= thr, k1 = u.y >= thr, k2 = u.z >= thr, k3 = u.w >= thr;
+  return __byte_perm(__byte_perm(k0, k1, 0x3340), __byte_perm(k2, k3, 0x3340), 0x5410);
+}
+
+// Mask bytes (one 0/1 byte per element, element e in byte e) of the 8
+// consecutive elements starting at global element index e0 (a multiple of 8).
+__device__ __forceinline__ uint2 keep_mask8(uint64_t e0, uint32_t thr, uint32_t k0, uint32_t k1,
+                                            uint32_t off0, uint32_t off1) {
+  const uint64_t q = e0 >> 2;
+  const uint4 a = philox4x32_10(
+      make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), off0, off1), k0, k1);
+  const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+                                           static_cast<uint32_t>((q + 1) >> 32), off0, off1),
+                                k0, k1);
+  return make_uint2(keep_bytes4(a, thr), keep_bytes4(b, thr));
+}
+
 // 8 mask bytes (0/1) from 8 keep bits.
 __device__ __forceinline__ uint2 bits_to_bytes8(uint32_t bits) {
   uint32_t lo = 0, hi = 0;
@@ -120,48 +139,34 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Shared-memory loads as ordinary C++ loads, so the compiler may schedule them
+// (the "memory" clobber of cp.async.wait_group still orders them after it).
 __device__ __forceinline__ uint4 lds16(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
+  return *reinterpret_cast<const uint4*>(p);
 }
 
 __device__ __forceinline__ uint2 lds8(const void* p) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
-  return v;
+  return *reinterpret_cast<const uint2*>(p);
 }
 
 // Read-only global load through the non-coherent path (small replicated
-// parameters: stays in L1 across rows).
+// parameters, re-read every row: kept in L1).
 __device__ __forceinline__ uint4 ldg16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+  return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// Streamed (read-once) global load: not allocated in L1.
+// Streamed (read-once) global load: evict-first.
 __device__ __forceinline__ uint4 ldg16_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+  return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
-// Streaming (write-once) global stores.
+// Streaming (write-once) global stores: evict-first.
 __device__ __forceinline__ void st16_stream(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
+  __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
 __device__ __forceinline__ void st8_stream(void* p, uint2 v) {
-  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};\n" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+  __stcs(reinterpret_cast<uint2*>(p), v);
 }
 
 // -------------------------------------------------------------- reductions --
@@ -199,17 +204,22 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 
 // ------------------------------------------------------------- shard map --
 // Token `row` = bi*s + si of the (b, s) grid -> its shard k and its row index
-// inside shard k's (b, s_k) tensor.
+// inside shard k's (b, s_k) tensor.  The offsets are non-decreasing, so the
+// shard of si is the number of offsets o_1..o_{t-1} at or below it (empty
+// shards are counted past); no division unless there are several batch rows.
 __device__ __forceinline__ void locate(const ShardMap& m, int64_t row, int& k, int64_t& local) {
   int64_t bi = 0, si = row;
   if (m.b > 1) {
-    bi = row / m.s;
+    if (row < (int64_t(1) << 32) && m.s < (int64_t(1) << 32)) {
+      bi = static_cast<uint32_t>(row) / static_cast<uint32_t>(m.s);
+    } else {
+      bi = row / m.s;
+    }
     si = row - bi * m.s;
   }
-  int kk = static_cast<int>((si * m.t) / m.s);
-  if (kk > m.t - 1) kk = m.t - 1;
-  while (kk + 1 < m.t && m.off[kk + 1] <= si) ++kk;
-  while (kk > 0 && m.off[kk] > si) --kk;
+  int kk = 0;
+#pragma unroll
+  for (int j = 1; j < SP_MAX_RANKS; ++j) kk += (j < m.t && m.off[j] <= si) ? 1 : 0;
   k = kk;
   local = bi * (m.off[kk + 1] - m.off[kk]) + (si - m.off[kk]);
 }

@@ -84,18 +84,19 @@ struct CopyParams {
 // Launch shapes chosen on the host.
 struct LaunchShape {
   int threads;     // threads per block (consumers of one token row)
-  int maxc;        // compile-time bound on chunks per row (1, 2, 4, 8)
-  int stages;      // cp.async pipeline depth
+  int maxc;        // chunks per row (backward: its compile-time bound)
+  int stages;      // cp.async pipeline depth (forward: chunks; backward: rows)
   int grid;        // blocks
   size_t smem;     // dynamic shared memory bytes
 };
 
 int device_sm_count();
 
-// Kernel entry of a (threads, chunks, stages) shape, or nullptr if that shape
-// is not instantiated.
-const void* fwd_kernel(int threads, int maxc, int stages);
-const void* bwd_kernel(int threads, int maxc, int stages);
+// Kernel entry of a launch shape, or nullptr if that shape is not instantiated.
+// Forward: (threads, ranks t, pipeline stages); backward: (threads, chunks per
+// row, ring rows).
+const void* fwd_kernel(int threads, int t, int stages);
+const void* bwd_kernel(int threads, int maxc, int ring);
 
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st);
 cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st);
