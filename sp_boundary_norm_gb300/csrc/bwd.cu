@@ -52,31 +52,35 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
     gam[ch] = (ch < nchunk && c < h) ? ldg16(P.gamma + c) : make_uint4(0, 0, 0, 0);
   }
 
-  // Stage row ri (all of its chunks, one cp.async group) into ring slot ri % RING.
-  auto issue_row = [&](int64_t ri) {
-    if (ri < nrows) {
-      int k;
-      int64_t local;
-      locate(P.map, blockIdx.x + ri * G, k, local);
-      uint8_t* base = smem + static_cast<size_t>(ri % RING) * MAXC * item_bytes;
+  // Stage row ri (all of its chunks, one cp.async group) into ring slot
+  // ri % RING; rows are issued in order, so one cursor walks them.
+  const int64_t c0 = tid * 8;
+  RowCursor pf;
+  pf.init(P.map, blockIdx.x);
+  int64_t pf_ri = 0;
+  auto issue_row = [&]() {
+    if (pf_ri < nrows) {
+      const int k = pf.k;
+      const int64_t lo0 = pf.local(P.map) * h + c0;
+      uint8_t* base = smem + static_cast<size_t>(pf_ri % RING) * MAXC * item_bytes;
 #pragma unroll
       for (int ch = 0; ch < MAXC; ++ch) {
-        const int64_t c = ch * kChunk + tid * 8;
-        if (ch < nchunk && c < h) {
+        if (ch < nchunk && ch * kChunk + c0 < h) {
           uint8_t* it = base + ch * item_bytes;
-          const int64_t lo = local * h + c;
+          const int64_t lo = lo0 + ch * kChunk;
           cp_async16(it + tid * 16, P.dy[k] + lo);
           cp_async16(it + v16 + tid * 16, P.z[k] + lo);
           if (has_skip) cp_async16(it + 2 * v16 + tid * 16, P.dz_skip[k] + lo);
           cp_async8(it + off_mask + tid * 8, P.mask[k] + lo);
         }
       }
+      if (++pf_ri < nrows) pf.advance(P.map, G);
     }
     cp_async_commit();
   };
 
 #pragma unroll
-  for (int i = 0; i < RING - 1; ++i) issue_row(i);
+  for (int i = 0; i < RING - 1; ++i) issue_row();
 
   float acc_g[MAXC][8], acc_b[MAXC][8], acc_bias[MAXC][8];
 #pragma unroll
@@ -85,55 +89,64 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
     for (int e = 0; e < 8; ++e) acc_g[ch][e] = acc_b[ch][e] = acc_bias[ch][e] = 0.f;
 
   // statistics of the current row, loaded one row ahead
+  RowCursor cur, nxt;
+  cur.init(P.map, blockIdx.x);
+  nxt = cur;
   float cur_mean = 0.f, cur_rstd = 0.f;
   if (nrows > 0) {
-    int k0;
-    int64_t l0;
-    locate(P.map, blockIdx.x, k0, l0);
-    cur_rstd = P.rstd[k0][l0];
-    if (is_ln) cur_mean = P.mean[k0][l0];
+    const int64_t l0 = cur.local(P.map);
+    cur_rstd = P.rstd[cur.k][l0];
+    if (is_ln) cur_mean = P.mean[cur.k][l0];
   }
 
   int slot_sel = 0;
   const float fh = static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
-    const int64_t row = blockIdx.x + ri * G;
-    int k;
-    int64_t local;
-    locate(P.map, row, k, local);
+    if (ri > 0) cur = nxt;
+    const int64_t row = cur.row;
+    const int k = cur.k;
+    const int64_t local = cur.local(P.map);
     float nx_mean = 0.f, nx_rstd = 0.f;
     if (ri + 1 < nrows) {
-      int k1;
-      int64_t l1;
-      locate(P.map, row + G, k1, l1);
-      nx_rstd = P.rstd[k1][l1];
-      if (is_ln) nx_mean = P.mean[k1][l1];
+      nxt.advance(P.map, G);
+      const int64_t l1 = nxt.local(P.map);
+      nx_rstd = P.rstd[nxt.k][l1];
+      if (is_ln) nx_mean = P.mean[nxt.k][l1];
     }
     const float mean = cur_mean, rstd = cur_rstd;
 
-    issue_row(ri + RING - 1);      // refills the slot row ri - 1 used
+    issue_row();                    // row ri + RING - 1 refills the slot row ri - 1 used
     cp_async_wait<RING - 1>();      // row ri has landed
     const uint8_t* base = smem + static_cast<size_t>(ri % RING) * MAXC * item_bytes;
 
     // ---- pass 1: the two row sums, and dgamma / dbeta terms --------------
+    // x_hat = (z - mean) * rstd (LN) or z * rstd (RMS); dxh = dY * gamma is an
+    // exact product of two bf16 values
+    const float nmean = -mean;
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
       const int64_t c = ch * kChunk + tid * 8;
       if (ch < nchunk && c < h) {
         const uint8_t* it = base + ch * item_bytes;
-        float dy[8], zf[8], g[8];
-        unpack8(lds16(it + tid * 16), dy);
-        unpack8(lds16(it + v16 + tid * 16), zf);
-        unpack8(gam[ch], g);
+        const uint4 dyv = lds16(it + tid * 16);
+        const uint4 zv = lds16(it + v16 + tid * 16);
+        float xh[8], dxh[8], dy[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float xh = is_ln ? (zf[e] - mean) * rstd : zf[e] * rstd;
-          const float dxh = dy[e] * g[e];
-          s1 += dxh;
-          s2 += dxh * xh;
-          acc_g[ch][e] += dy[e] * xh;
-          acc_b[ch][e] += dy[e];
+          xh[e] = is_ln ? nmean : 0.f;
+          dxh[e] = 0.f;
+        }
+        add8_bf16(zv, xh);
+        fma8_bf16(dyv, gam[ch], dxh);
+        add8_bf16(dyv, acc_b[ch]);
+        unpack8(dyv, dy);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          xh[e] *= rstd;
+          s1 += dxh[e];
+          s2 = fmaf(dxh[e], xh[e], s2);
+          acc_g[ch][e] = fmaf(dy[e], xh[e], acc_g[ch][e]);
         }
       }
     }
@@ -149,24 +162,25 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
       const int64_t c = ch * kChunk + tid * 8;
       if (ch < nchunk && c < h) {
         const uint8_t* it = base + ch * item_bytes;
-        float dy[8], zf[8], g[8], sk[8], dz[8], dp[8];
-        unpack8(lds16(it + tid * 16), dy);
-        unpack8(lds16(it + v16 + tid * 16), zf);
-        unpack8(gam[ch], g);
-        if (has_skip) {
-          unpack8(lds16(it + 2 * v16 + tid * 16), sk);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) sk[e] = 0.f;
-        }
+        const uint4 dyv = lds16(it + tid * 16);
+        const uint4 zv = lds16(it + v16 + tid * 16);
         const uint2 mk = lds8(it + off_mask + tid * 8);
+        float xh[8], dz[8], dp[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float xh = is_ln ? (zf[e] - mean) * rstd : zf[e] * rstd;
-          const float dxh = dy[e] * g[e];
-          dz[e] = rstd * (dxh - m1 - xh * m2) + sk[e];
-          const uint32_t kb = ((e < 4 ? mk.x : mk.y) >> (8 * (e & 3))) & 0xFFu;
-          dp[e] = kb ? dz[e] * P.scale : 0.f;
+          xh[e] = is_ln ? nmean : 0.f;
+          dz[e] = -m1;
+        }
+        add8_bf16(zv, xh);
+        fma8_bf16(dyv, gam[ch], dz);            // dxh - m1
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dz[e] = rstd * fmaf(-xh[e] * rstd, m2, dz[e]);
+        if (has_skip) add8_bf16(lds16(it + 2 * v16 + tid * 16), dz);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          // mask bytes are 0 or 1: bit 0 of byte e decides
+          const bool kept = ((e < 4 ? mk.x : mk.y) & (1u << (8 * (e & 3)))) != 0u;
+          dp[e] = kept ? dz[e] * P.scale : 0.f;
           acc_bias[ch][e] += dp[e];
         }
         st16_stream(P.dresidual[k] + local * h + c, pack8(dz));

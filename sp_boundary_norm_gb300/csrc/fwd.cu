@@ -30,40 +30,47 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
   const int tid = threadIdx.x;
   const int t = TT > 0 ? TT : P.map.t;     // compile-time rank count when specialised
   const int64_t h = P.map.h;
-  constexpr int64_t kChunk = 8LL * NTHR;
+  constexpr int kChunk = 8 * NTHR;
   const int nchunk = static_cast<int>((h + kChunk - 1) / kChunk);
-  constexpr size_t kStream = static_cast<size_t>(NTHR) * 16;
-  const size_t stage_bytes = static_cast<size_t>(t + 1) * kStream;
-  uint8_t* zbuf = smem + STAGES * stage_bytes;                       // [nchunk][NTHR][16 B]
-  float* red = reinterpret_cast<float*>(zbuf + nchunk * kStream);   // [2][32]
+  constexpr int kStream = NTHR * 16;
+  const int stage_bytes = (t + 1) * kStream;
+  uint8_t* zbuf = smem + STAGES * stage_bytes + tid * 16;   // own slots, stride kStream
+  float* red = reinterpret_cast<float*>(smem + STAGES * stage_bytes + nchunk * kStream);
   const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
   const int64_t G = gridDim.x;
   const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
+  const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
 
   // ---- prefetch cursor: the next (row, chunk) item to stage -------------
-  int64_t pf_ri = 0;
-  int pf_chunk = 0, pf_stage = 0, pf_k = 0;
-  int64_t pf_local = 0;
-  if (nrows > 0) locate(P.map, blockIdx.x, pf_k, pf_local);
+  // pf_goff: element offset of (row, chunk) in the (b, s, h) partials;
+  // pf_roff: element offset in the residual shard of that row.
+  RowCursor pf;
+  pf.init(P.map, blockIdx.x);
+  int64_t pf_ri = 0, pf_goff = pf.row * h + c0, pf_roff = pf.local(P.map) * h + c0;
+  int pf_chunk = 0, pf_stage = 0;
 
   auto issue_next = [&]() {
     if (pf_ri < nrows) {
-      const int64_t row = blockIdx.x + pf_ri * G;
-      const int64_t c = pf_chunk * kChunk + tid * 8;
-      if (c < h) {
+      if (pf_chunk * kChunk + c0 < h) {
         uint8_t* slot = smem + pf_stage * stage_bytes + tid * 16;
-        const int64_t goff = row * h + c;
 #pragma unroll
         for (int r = 0; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
-          if (TT > 0 || r < t) cp_async16(slot + r * kStream, P.partials[r] + goff);
-        cp_async16(slot + t * kStream, P.residual[pf_k] + pf_local * h + c);
+          if (TT > 0 || r < t) cp_async16(slot + r * kStream, P.partials[r] + pf_goff);
+        cp_async16(slot + t * kStream, P.residual[pf.k] + pf_roff);
       }
       if (++pf_chunk == nchunk) {
         pf_chunk = 0;
-        if (++pf_ri < nrows) locate(P.map, blockIdx.x + pf_ri * G, pf_k, pf_local);
+        if (++pf_ri < nrows) {
+          pf.advance(P.map, G);
+          pf_goff = pf.row * h + c0;
+          pf_roff = pf.local(P.map) * h + c0;
+        }
+      } else {
+        pf_goff += kChunk;
+        pf_roff += kChunk;
       }
     }
     cp_async_commit();
@@ -73,16 +80,19 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
 #pragma unroll
   for (int i = 0; i < STAGES - 1; ++i) issue_next();
 
+  RowCursor cur;
+  cur.init(P.map, blockIdx.x);
   int stage = 0;
   int slot_sel = 0;
   const float fh = static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
-    const int64_t row = blockIdx.x + ri * G;
-    int k;
-    int64_t local;
-    locate(P.map, row, k, local);
-    uint16_t* zrow = P.z[k] + local * h;
-    uint8_t* mrow = P.mask[k] + local * h;
+    if (ri > 0) cur.advance(P.map, G);
+    const int64_t row = cur.row;
+    const int k = cur.k;
+    const int64_t local = cur.local(P.map);
+    uint16_t* zrow = P.z[k] + local * h + c0;
+    uint8_t* mrow = P.mask[k] + local * h + c0;
+    const uint64_t e_row = static_cast<uint64_t>(row * h + c0);   // global element index
 
     // ---- pass 1: g* sum, bias, dropout, residual -> Z (stored) ----------
     float lsum = 0.f;
@@ -90,43 +100,54 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
     for (int ch = 0; ch < nchunk; ++ch) {
       issue_next();
       cp_async_wait<STAGES - 1>();
-      const int64_t c = ch * kChunk + tid * 8;
-      if (c < h) {
+      const int cc = ch * kChunk;
+      if (cc + c0 < h) {
         const uint8_t* slot = smem + stage * stage_bytes + tid * 16;
-        const uint4 bv = ldg16(P.bias + c);
-        uint2 keep = make_uint2(0x01010101u, 0x01010101u);
-        if (P.thr) keep = keep_mask8(static_cast<uint64_t>(row * h + c), P.thr, P.key0, P.key1,
-                                     P.off0, P.off1);
+        const uint4 bv = ldg16(P.bias + cc + c0);
         // g*: float32 sum of the t partials, ranks in ascending order
-        float y[8], q[8];
+        // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
+        float y[8];
         unpack8(lds16(slot), y);
 #pragma unroll
-        for (int r = 1; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r) {
-          if (TT > 0 || r < t) {
-            unpack8(lds16(slot + r * kStream), q);
+        for (int r = 1; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
+          if (TT > 0 || r < t) add8_bf16(lds16(slot + r * kStream), y);
+        add8_bf16(bv, y);   // + bias
+        // dropout: element e keeps iff its Philox word >= thr
+        uint2 keep = make_uint2(0x01010101u, 0x01010101u);
+        if (P.thr) {
+          const uint64_t q = (e_row + cc) >> 2;
+          const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
+                                                   static_cast<uint32_t>(q >> 32), P.off0, P.off1),
+                                        P.key0, P.key1);
+          const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+                                                   static_cast<uint32_t>((q + 1) >> 32), P.off0,
+                                                   P.off1),
+                                        P.key0, P.key1);
+          const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], q[e]);
-          }
+          for (int e = 0; e < 8; ++e) y[e] = (u[e] >= P.thr) ? __fmul_rn(y[e], P.scale) : 0.f;
+          keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         }
-        unpack8(bv, q);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], q[e]);
-        unpack8(lds16(slot + t * kStream), q);   // residual
-        float zr[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t kb = ((e < 4 ? keep.x : keep.y) >> (8 * (e & 3))) & 0xFFu;
-          const float d = kb ? __fmul_rn(y[e], P.scale) : 0.f;
-          zr[e] = __fadd_rn(d, q[e]);
+        // (with p == 0 the scale is exactly 1 and y * 1 == y)
+        add8_bf16(lds16(slot + t * kStream), y);   // + residual -> Z in fp32
+        const uint4 zb = pack8(y);                 // Z = bf16_rne(...)
+        st16_stream(zrow + cc, zb);
+        st8_stream(mrow + cc, keep);
+        *reinterpret_cast<uint4*>(zbuf + ch * kStream) = zb;
+        // the norm sees the stored bf16 values
+        float l2[2] = {0.f, 0.f};
+        if (is_ln) {
+          add2_bf16(zb.x, l2[0], l2[1]);
+          add2_bf16(zb.y, l2[0], l2[1]);
+          add2_bf16(zb.z, l2[0], l2[1]);
+          add2_bf16(zb.w, l2[0], l2[1]);
+        } else {
+          fma2_bf16(zb.x, zb.x, l2[0], l2[1]);
+          fma2_bf16(zb.y, zb.y, l2[0], l2[1]);
+          fma2_bf16(zb.z, zb.z, l2[0], l2[1]);
+          fma2_bf16(zb.w, zb.w, l2[0], l2[1]);
         }
-        const uint4 zb = pack8(zr);
-        st16_stream(zrow + c, zb);
-        st8_stream(mrow + c, keep);
-        *reinterpret_cast<uint4*>(zbuf + ch * kStream + tid * 16) = zb;
-        float zf[8];
-        unpack8(zb, zf);   // the norm sees the stored bf16 values
-#pragma unroll
-        for (int e = 0; e < 8; ++e) lsum += is_ln ? zf[e] : zf[e] * zf[e];
+        lsum += l2[0] + l2[1];
       }
       stage = (stage + 1 == STAGES) ? 0 : stage + 1;
     }
@@ -137,16 +158,14 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
       mean = block_sum(lsum, red + 32 * slot_sel) / fh;
       slot_sel ^= 1;
       float lsq = 0.f;
+      const float nmean = -mean;
 #pragma unroll 1
       for (int ch = 0; ch < nchunk; ++ch) {
-        if (ch * kChunk + tid * 8 < h) {
-          float zf[8];
-          unpack8(lds16(zbuf + ch * kStream + tid * 16), zf);
+        if (ch * kChunk + c0 < h) {
+          float d[8] = {nmean, nmean, nmean, nmean, nmean, nmean, nmean, nmean};
+          add8_bf16(lds16(zbuf + ch * kStream), d);   // z - mean
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float d = zf[e] - mean;
-            lsq += d * d;
-          }
+          for (int e = 0; e < 8; ++e) lsq = fmaf(d[e], d[e], lsq);
         }
       }
       const float var = block_sum(lsq, red + 32 * slot_sel) / fh;
@@ -159,24 +178,32 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
     }
 
     // ---- normalise and write into the all-gather destination(s) ----------
+    const int64_t orow = row * h + c0;
 #pragma unroll 1
     for (int ch = 0; ch < nchunk; ++ch) {
-      const int64_t c = ch * kChunk + tid * 8;
-      if (c < h) {
-        float zf[8], g[8], o[8];
-        unpack8(lds16(zbuf + ch * kStream + tid * 16), zf);
-        unpack8(ldg16(P.gamma + c), g);
+      const int cc = ch * kChunk;
+      if (cc + c0 < h) {
+        const uint4 zv = lds16(zbuf + ch * kStream);
+        const uint4 gv = ldg16(P.gamma + cc + c0);
+        float o[8];
         if (is_ln) {
-          float bt[8];
-          unpack8(ldg16(P.beta + c), bt);
+          float g[8], bt[8];
+          unpack8(gv, g);
+          unpack8(ldg16(P.beta + cc + c0), bt);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = fmaf((zf[e] - mean) * rstd, g[e], bt[e]);
+          for (int e = 0; e < 8; ++e) o[e] = -mean;
+          add8_bf16(zv, o);   // z - mean
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = fmaf(o[e] * rstd, g[e], bt[e]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = (zf[e] * rstd) * g[e];
+          for (int e = 0; e < 8; ++e) o[e] = 0.f;
+          fma8_bf16(zv, gv, o);   // z * gamma, exact
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] *= rstd;
         }
         const uint4 ob = pack8(o);
-        for (int j = 0; j < P.n_gather; ++j) st16_stream(P.gathered[j] + row * h + c, ob);
+        for (int j = 0; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
       }
     }
     if (tid == 0) {

@@ -19,11 +19,11 @@ __global__ void __launch_bounds__(kCopyThreads) allgather_kernel(const CopyParam
     check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
   const int64_t h = P.map.h;
   const int64_t nvec = h / 8;
+  RowCursor cur;
+  cur.init(P.map, blockIdx.x);
   for (int64_t row = blockIdx.x; row < P.rows; row += gridDim.x) {
-    int k;
-    int64_t local;
-    locate(P.map, row, k, local);
-    const uint16_t* src = P.src[k] + local * h;
+    if (row != blockIdx.x) cur.advance(P.map, gridDim.x);
+    const uint16_t* src = P.src[cur.k] + cur.local(P.map) * h;
     for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += kCopyThreads * kCopyUnroll) {
       uint4 buf[kCopyUnroll];
 #pragma unroll
@@ -48,11 +48,11 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_scatter_kernel(const Copy
     check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
   const int64_t h = P.map.h;
   const int64_t nvec = h / 8;
+  RowCursor cur;
+  cur.init(P.map, blockIdx.x);
   for (int64_t row = blockIdx.x; row < P.rows; row += gridDim.x) {
-    int k;
-    int64_t local;
-    locate(P.map, row, k, local);
-    uint16_t* dst = P.dst[k] + local * h;
+    if (row != blockIdx.x) cur.advance(P.map, gridDim.x);
+    uint16_t* dst = P.dst[cur.k] + cur.local(P.map) * h;
     for (int64_t v = threadIdx.x; v < nvec; v += kCopyThreads) {
       const int64_t off = row * h + v * 8;
       float y[8], q[8];

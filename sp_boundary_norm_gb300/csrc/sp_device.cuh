@@ -70,6 +70,49 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
+// ------------------------------------------- mixed bf16 / fp32 arithmetic --
+// sm_100-class mixed-precision add / fma: bf16 operands are widened exactly
+// inside the instruction and the fp32 result is rounded once (round to
+// nearest even), so add_bf16(a, c) == __fadd_rn(float(a), c) bit for bit.
+// A 32-bit register holds two bf16: element 2i in the low half.
+
+// c[0] += lo(v), c[1] += hi(v)
+__device__ __forceinline__ void add2_bf16(uint32_t v, float& c0, float& c1) {
+  asm("{.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(v));
+}
+
+// c[e] += bf16 element e of v (8 elements)
+__device__ __forceinline__ void add8_bf16(const uint4 v, float c[8]) {
+  add2_bf16(v.x, c[0], c[1]);
+  add2_bf16(v.y, c[2], c[3]);
+  add2_bf16(v.z, c[4], c[5]);
+  add2_bf16(v.w, c[6], c[7]);
+}
+
+// c[e] = a[e] * b[e] + c[e] with a, b bf16 (the product of two bf16 is exact
+// in fp32, so with c == 0 this is the exact product)
+__device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t b, float& c0, float& c1) {
+  asm("{.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, ah, bh, %1;}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(a), "r"(b));
+}
+
+__device__ __forceinline__ void fma8_bf16(const uint4 a, const uint4 b, float c[8]) {
+  fma2_bf16(a.x, b.x, c[0], c[1]);
+  fma2_bf16(a.y, b.y, c[2], c[3]);
+  fma2_bf16(a.z, b.z, c[4], c[5]);
+  fma2_bf16(a.w, b.w, c[6], c[7]);
+}
+
 // Keep flags (0/1) of 4 draws against thr, and their 4 mask bytes.
 __device__ __forceinline__ uint32_t keep_bytes4(uint4 u, uint32_t thr) {
   const uint32_t k0 = u.x >= thr, k1 = u.y >= thr, k2 = u.z >= thr, k3 = u.w >= thr;
@@ -176,16 +219,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Block-wide sum in a fixed order (deterministic).  `red` is a 32-float
-// shared slot; two consecutive calls must use different slots.
+// Block-wide sums in a fixed order (deterministic): warp butterflies, one
+// partial per warp in shared memory, then every warp runs the same butterfly
+// over those partials, so all threads get the same bits.  `red` is a
+// 32-entry shared slot; two consecutive calls must use different slots.
 __device__ __forceinline__ float block_sum(float v, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   v = warp_sum(v);
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  float s = 0.f;
-  for (int i = 0; i < nw; ++i) s += red[i];
-  return s;
+  return warp_sum(lane < nw ? red[lane] : 0.f);
 }
 
 __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
@@ -194,35 +237,45 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
   b = warp_sum(b);
   if (lane == 0) red[warp] = make_float2(a, b);
   __syncthreads();
-  float2 s = make_float2(0.f, 0.f);
-  for (int i = 0; i < nw; ++i) {
-    s.x += red[i].x;
-    s.y += red[i].y;
-  }
-  return s;
+  const float2 p = lane < nw ? red[lane] : make_float2(0.f, 0.f);
+  return make_float2(warp_sum(p.x), warp_sum(p.y));
 }
 
 // ------------------------------------------------------------- shard map --
-// Token `row` = bi*s + si of the (b, s) grid -> its shard k and its row index
-// inside shard k's (b, s_k) tensor.  The offsets are non-decreasing, so the
-// shard of si is the number of offsets o_1..o_{t-1} at or below it (empty
-// shards are counted past); no division unless there are several batch rows.
-__device__ __forceinline__ void locate(const ShardMap& m, int64_t row, int& k, int64_t& local) {
-  int64_t bi = 0, si = row;
-  if (m.b > 1) {
-    if (row < (int64_t(1) << 32) && m.s < (int64_t(1) << 32)) {
-      bi = static_cast<uint32_t>(row) / static_cast<uint32_t>(m.s);
-    } else {
-      bi = row / m.s;
-    }
-    si = row - bi * m.s;
+// Position of token `row` = bi*s + si of the (b, s) grid: its shard k (the
+// shard holding positions [o_k, o_{k+1}) of each batch row) and its row index
+// inside shard k's (b, s_k) tensor.  A persistent block visits rows
+// r, r + G, r + 2G, ..., so the cursor advances incrementally: the shard index
+// only moves forward within a batch row, and a division happens only when a
+// step crosses into another batch row.
+struct RowCursor {
+  int64_t row, bi, si;
+  int k;
+
+  __device__ __forceinline__ void seek_shard(const ShardMap& m) {
+    while (k + 1 < m.t && m.off[k + 1] <= si) ++k;
   }
-  int kk = 0;
-#pragma unroll
-  for (int j = 1; j < SP_MAX_RANKS; ++j) kk += (j < m.t && m.off[j] <= si) ? 1 : 0;
-  k = kk;
-  local = bi * (m.off[kk + 1] - m.off[kk]) + (si - m.off[kk]);
-}
+  __device__ __forceinline__ void init(const ShardMap& m, int64_t r) {
+    row = r;
+    bi = (m.b > 1) ? r / m.s : 0;
+    si = r - bi * m.s;
+    k = 0;
+    seek_shard(m);
+  }
+  __device__ __forceinline__ void advance(const ShardMap& m, int64_t stride) {
+    row += stride;
+    si += stride;
+    if (si >= m.s) {
+      bi += si / m.s;
+      si %= m.s;
+      k = 0;
+    }
+    seek_shard(m);
+  }
+  __device__ __forceinline__ int64_t local(const ShardMap& m) const {
+    return bi * (m.off[k + 1] - m.off[k]) + (si - m.off[k]);
+  }
+};
 
 // Device check of packed-sequence metadata: cu_seqlens[0] == 0, non-decreasing,
 // cu_seqlens[n] == total.  Run by one warp; flags SP_ERR_DEVICE_CHECK.
