@@ -223,7 +223,7 @@ LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip) {
   const size_t item = static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + threads * 8;
   const size_t ring_row = item * maxc;
   return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 3,
-                    /*ring=*/3, /*blocks per SM=*/threads == 512 ? 1 : 2,
+                    /*ring=*/2, /*blocks per SM=*/threads == 512 ? 1 : 2,
                     [&](int st) { return bwd_kernel(threads, maxc, st); });
 }
 

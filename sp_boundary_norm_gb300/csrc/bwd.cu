@@ -58,11 +58,12 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   RowCursor pf;
   pf.init(P.map, blockIdx.x);
   int64_t pf_ri = 0;
+  int pf_slot = 0;
   auto issue_row = [&]() {
     if (pf_ri < nrows) {
       const int k = pf.k;
       const int64_t lo0 = pf.local(P.map) * h + c0;
-      uint8_t* base = smem + static_cast<size_t>(pf_ri % RING) * MAXC * item_bytes;
+      uint8_t* base = smem + pf_slot * MAXC * static_cast<int>(item_bytes);
 #pragma unroll
       for (int ch = 0; ch < MAXC; ++ch) {
         if (ch < nchunk && ch * kChunk + c0 < h) {
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
       if (++pf_ri < nrows) pf.advance(P.map, G);
     }
     cp_async_commit();
+    pf_slot = (pf_slot + 1 == RING) ? 0 : pf_slot + 1;
   };
 
 #pragma unroll
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   }
 
   int slot_sel = 0;
+  int slot = 0;   // ring slot of the current row
   const float fh = static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
     if (ri > 0) cur = nxt;
@@ -117,29 +120,24 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
 
     issue_row();                    // row ri + RING - 1 refills the slot row ri - 1 used
     cp_async_wait<RING - 1>();      // row ri has landed
-    const uint8_t* base = smem + static_cast<size_t>(ri % RING) * MAXC * item_bytes;
+    const uint8_t* base = smem + slot * MAXC * static_cast<int>(item_bytes) + tid * 16;
+    slot = (slot + 1 == RING) ? 0 : slot + 1;
 
     // ---- pass 1: the two row sums, and dgamma / dbeta terms --------------
     // x_hat = (z - mean) * rstd (LN) or z * rstd (RMS); dxh = dY * gamma is an
     // exact product of two bf16 values
-    const float nmean = -mean;
+    const float nmean = is_ln ? -mean : 0.f;
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
-      const int64_t c = ch * kChunk + tid * 8;
-      if (ch < nchunk && c < h) {
+      if (ch < nchunk && ch * kChunk + c0 < h) {
         const uint8_t* it = base + ch * item_bytes;
-        const uint4 dyv = lds16(it + tid * 16);
-        const uint4 zv = lds16(it + v16 + tid * 16);
+        const uint4 dyv = lds16(it);
+        const uint4 zv = lds16(it + v16);
         float xh[8], dxh[8], dy[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          xh[e] = is_ln ? nmean : 0.f;
-          dxh[e] = 0.f;
-        }
-        add8_bf16(zv, xh);
-        fma8_bf16(dyv, gam[ch], dxh);
-        add8_bf16(dyv, acc_b[ch]);
+        add8_bf16_bcast(zv, nmean, xh);
+        fma8_bf16_bcast(dyv, gam[ch], 0.f, dxh);
+        if (is_ln) add8_bf16(dyv, acc_b[ch]);
         unpack8(dyv, dy);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -153,29 +151,27 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
 
     const float2 s = block_sum2(s1, s2, red + 32 * slot_sel);
     slot_sel ^= 1;
-    const float m1 = is_ln ? s.x / fh : 0.f;
-    const float m2 = s.y / fh;
+    const float nm1 = is_ln ? -(s.x / fh) : 0.f;
+    const float m2r = (s.y / fh) * rstd;
 
     // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
+    // dZ = rstd * (dxh - m1 - (z - mean) * rstd * m2)
+    uint16_t* dres_row = P.dresidual[k] + local * h + c0;
+    const int64_t grow = row * h + c0;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
-      const int64_t c = ch * kChunk + tid * 8;
-      if (ch < nchunk && c < h) {
+      const int cc = ch * static_cast<int>(kChunk);
+      if (ch < nchunk && cc + c0 < h) {
         const uint8_t* it = base + ch * item_bytes;
-        const uint4 dyv = lds16(it + tid * 16);
-        const uint4 zv = lds16(it + v16 + tid * 16);
-        const uint2 mk = lds8(it + off_mask + tid * 8);
-        float xh[8], dz[8], dp[8];
+        const uint4 dyv = lds16(it);
+        const uint4 zv = lds16(it + v16);
+        const uint2 mk = lds8(it + off_mask - tid * 8);   // mask slots are 8 B apart
+        float zc[8], dz[8], dp[8];
+        add8_bf16_bcast(zv, nmean, zc);           // z - mean
+        fma8_bf16_bcast(dyv, gam[ch], nm1, dz);  // dxh - m1
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          xh[e] = is_ln ? nmean : 0.f;
-          dz[e] = -m1;
-        }
-        add8_bf16(zv, xh);
-        fma8_bf16(dyv, gam[ch], dz);            // dxh - m1
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dz[e] = rstd * fmaf(-xh[e] * rstd, m2, dz[e]);
-        if (has_skip) add8_bf16(lds16(it + 2 * v16 + tid * 16), dz);
+        for (int e = 0; e < 8; ++e) dz[e] = rstd * fmaf(-zc[e], m2r, dz[e]);
+        if (has_skip) add8_bf16(lds16(it + 2 * v16), dz);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           // mask bytes are 0 or 1: bit 0 of byte e decides
@@ -183,9 +179,9 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
           dp[e] = kept ? dz[e] * P.scale : 0.f;
           acc_bias[ch][e] += dp[e];
         }
-        st16_stream(P.dresidual[k] + local * h + c, pack8(dz));
+        st16_stream(dres_row + cc, pack8(dz));
         const uint4 pb = pack8(dp);
-        for (int j = 0; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + row * h + c, pb);
+        for (int j = 0; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + cc, pb);
       }
     }
     cur_mean = nx_mean;

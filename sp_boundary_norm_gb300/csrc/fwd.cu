@@ -162,8 +162,8 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
 #pragma unroll 1
       for (int ch = 0; ch < nchunk; ++ch) {
         if (ch * kChunk + c0 < h) {
-          float d[8] = {nmean, nmean, nmean, nmean, nmean, nmean, nmean, nmean};
-          add8_bf16(lds16(zbuf + ch * kStream), d);   // z - mean
+          float d[8];
+          add8_bf16_bcast(lds16(zbuf + ch * kStream), nmean, d);   // z - mean
 #pragma unroll
           for (int e = 0; e < 8; ++e) lsq = fmaf(d[e], d[e], lsq);
         }
@@ -190,15 +190,11 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
           float g[8], bt[8];
           unpack8(gv, g);
           unpack8(ldg16(P.beta + cc + c0), bt);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = -mean;
-          add8_bf16(zv, o);   // z - mean
+          add8_bf16_bcast(zv, -mean, o);   // z - mean
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = fmaf(o[e] * rstd, g[e], bt[e]);
         } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = 0.f;
-          fma8_bf16(zv, gv, o);   // z * gamma, exact
+          fma8_bf16_bcast(zv, gv, 0.f, o);   // z * gamma, exact
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] *= rstd;
         }

@@ -94,6 +94,40 @@ __device__ __forceinline__ void add8_bf16(const uint4 v, float c[8]) {
   add2_bf16(v.w, c[6], c[7]);
 }
 
+// d0 = lo(v) + c0, d1 = hi(v) + c1 (non-destructive: no copy of c needed)
+__device__ __forceinline__ void add2_bf16_to(uint32_t v, float c0, float c1, float& d0,
+                                             float& d1) {
+  asm("{.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %3;\n\t"
+      "add.rn.f32.bf16 %1, hi, %4;}"
+      : "=f"(d0), "=f"(d1)
+      : "r"(v), "f"(c0), "f"(c1));
+}
+
+// d[e] = bf16 element e of v + c (the same c for all 8)
+__device__ __forceinline__ void add8_bf16_bcast(const uint4 v, float c, float d[8]) {
+  add2_bf16_to(v.x, c, c, d[0], d[1]);
+  add2_bf16_to(v.y, c, c, d[2], d[3]);
+  add2_bf16_to(v.z, c, c, d[4], d[5]);
+  add2_bf16_to(v.w, c, c, d[6], d[7]);
+}
+
+// d[e] = a[e] * b[e] + c (bf16 a, b; the same c for all 8)
+__device__ __forceinline__ void fma8_bf16_bcast(const uint4 a, const uint4 b, float c,
+                                                float d[8]) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %4;\n\t"
+        "fma.rn.f32.bf16 %1, ah, bh, %4;}"
+        : "=f"(d[2 * i]), "=f"(d[2 * i + 1])
+        : "r"(av[i]), "r"(bv[i]), "f"(c));
+}
+
 // c[e] = a[e] * b[e] + c[e] with a, b bf16 (the product of two bf16 is exact
 // in fp32, so with c == 0 this is the exact product)
 __device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t b, float& c0, float& c1) {
