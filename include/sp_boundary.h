@@ -192,6 +192,40 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         void* stream);
 
+/*
+ * sp_norm_bwd_noalloc -- sp_norm_bwd for callers that cannot allocate device
+ * memory.  The lesson has no counterpart to this entry point: it exists for
+ * callers that cannot obtain a workspace themselves, such as a plugin inside
+ * a host framework that reserves all device memory up front and hands its
+ * plugins no scratch, or a path where cudaMalloc's implicit device
+ * synchronisation is not acceptable.
+ *
+ * Arguments and results are those of sp_norm_bwd, minus the workspace.  The
+ * per-block parameter-gradient partials go to a fixed array in the library's
+ * own device memory (SP_NOALLOC_WORKSPACE_BYTES on every GPU that loads the
+ * library, held until the process exits).  Nothing is allocated or freed by
+ * the call.
+ *  - Shapes whose workspace (sp_norm_bwd_workspace_bytes) exceeds
+ *    SP_NOALLOC_WORKSPACE_BYTES are rejected with SP_ERR_UNSUPPORTED before
+ *    anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture
+ *    on that device.
+ *  - All calls on a device share the one array: calls that may overlap on the
+ *    GPU (different streams, no ordering between them) race on it.  Serialise
+ *    them (one stream, or events).  Every call overwrites the partials it
+ *    reads, so no clearing is needed between calls.
+ */
+#define SP_NOALLOC_WORKSPACE_BYTES (16u << 20)
+sp_status_t sp_norm_bwd_noalloc(const void* const* dy, const void* const* z,
+                                const uint8_t* const* mask, const float* const* mean,
+                                const float* const* rstd, const void* gamma,
+                                const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                                int32_t t, double p, const int32_t* cu_seqlens,
+                                int32_t n_seqs, sp_norm_t norm, void* const* dresidual,
+                                void* const* dgathered, int32_t n_gather, float* dgamma,
+                                float* dbeta, float* dbias, int32_t* dev_status, void* stream);
+
 /* Thread-local text of the last non-OK status returned on this thread. */
 const char* sp_last_error(void);
 

@@ -61,6 +61,10 @@ def load():
     lib.sp_norm_bwd.argtypes = [
         _PP, _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _vp, _i32,
         _i32, _PP, _PP, _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+    lib.sp_norm_bwd_noalloc.restype = _i32
+    lib.sp_norm_bwd_noalloc.argtypes = [
+        _PP, _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _vp, _i32,
+        _i32, _PP, _PP, _i32, _vp, _vp, _vp, _vp, _vp]
     lib.sp_last_error.restype = ctypes.c_char_p
     lib.sp_last_error.argtypes = []
     lib.sp_abi_version.restype = _i32
@@ -260,6 +264,54 @@ def sp_norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlen
         NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
         _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev))
+    _check(code)
+
+
+NOALLOC_WORKSPACE_BYTES = 16 << 20
+
+
+def sp_norm_bwd_noalloc(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlens=None,
+                        norm="layernorm", dresidual, dgathered, dgamma=None, dbeta=None,
+                        dbias=None, status=None):
+    """sp_norm_bwd for callers that cannot allocate: no workspace argument.
+
+    The library keeps the parameter-gradient partials in a fixed array of its
+    own device memory (16 MiB per GPU, for the life of the process), so a
+    caller that has no allocator to draw scratch from can still run the
+    backward.  Calls on one device share that array: do not let two of them
+    run concurrently on different streams.  The first call on a device looks
+    up the array's address; make it before any stream capture.
+    """
+    lib = load()
+    t = len(dy)
+    b, _, h = dy[0].shape
+    dev = dy[0].device
+    bf = torch.bfloat16
+    sizes = shard_sizes(s, t)
+    ln = norm == "layernorm"
+    for k in range(t):
+        _need(dy[k], (b, sizes[k], h), bf, dev, f"dy[{k}]")
+        _need(z[k], (b, sizes[k], h), bf, dev, f"z[{k}]")
+        _need(mask[k], (b, sizes[k], h), torch.uint8, dev, f"mask[{k}]")
+        _need(rstd[k], (b, sizes[k]), torch.float32, dev, f"rstd[{k}]")
+        if ln:
+            _need(mean[k], (b, sizes[k]), torch.float32, dev, f"mean[{k}]")
+        if dz_skip is not None:
+            _need(dz_skip[k], (b, sizes[k], h), bf, dev, f"dz_skip[{k}]")
+        _need(dresidual[k], (b, sizes[k], h), bf, dev, f"dresidual[{k}]")
+    for j, g in enumerate(dgathered):
+        _need(g, (b, s, h), bf, dev, f"dgathered[{j}]")
+    _need(gamma, (h,), bf, dev, "gamma")
+    for name, v in (("dgamma", dgamma), ("dbeta", dbeta), ("dbias", dbias)):
+        if v is not None:
+            _need(v, (h,), torch.float32, dev, name)
+    cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
+    st = device_status(dev) if status is None else status
+    code = lib.sp_norm_bwd_noalloc(
+        _ptr_array(dy), _ptr_array(z), _ptr_array(mask), _ptr_array(mean) if ln else None,
+        _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), cu, n_seqs,
+        NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
+        _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(st), _stream(dev))
     _check(code)
 
 

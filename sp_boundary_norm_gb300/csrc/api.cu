@@ -239,6 +239,10 @@ cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStre
 
 }  // namespace
 
+sp_status_t record_error(sp_status_t code, const char* message) {
+  return fail(code, "%s", message);
+}
+
 int device_sm_count() {
   static std::mutex mu;
   static int cache[64] = {0};

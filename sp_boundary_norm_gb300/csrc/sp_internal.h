@@ -92,6 +92,9 @@ struct LaunchShape {
 
 int device_sm_count();
 
+// Sets the thread's sp_last_error() text; returns `code`.
+sp_status_t record_error(sp_status_t code, const char* message);
+
 // Kernel entry of a launch shape, or nullptr if that shape is not instantiated.
 // Forward: (threads, ranks t, pipeline stages); backward: (threads, chunks per
 // row, ring rows).
