@@ -336,6 +336,11 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     if args.s:
         w = w.with_(s=args.s, name=f"{w.name}-s{args.s}")
+    if args.p is not None:
+        w = w.with_(p=args.p, name=f"{w.name}-p{args.p}")
+    if args.norm is not None:
+        w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
+                    name=f"{w.name}-{args.norm}")
     step = Step(w, device, n_gather=args.n_gather)
     total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world, device)
     rejected = False
@@ -461,6 +466,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="70b", choices=["70b", "trace4k", "ragged", "tiny"])
     ap.add_argument("--s", type=int, default=0,
                     help="override the sequence length (smaller cases for profiling)")
+    ap.add_argument("--p", type=float, default=None, help="override the dropout probability")
+    ap.add_argument("--norm", choices=["layernorm", "rmsnorm"], default=None,
+                    help="override the norm")
     ap.add_argument("--n-gather", type=int, default=1)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -28,16 +28,23 @@ template <int NTHR, int MAXC, int RING>
 __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
-  const int64_t h = P.map.h;
-  constexpr int64_t kChunk = 8LL * NTHR;
-  const int nchunk = static_cast<int>((h + kChunk - 1) / kChunk);
+  const int h = static_cast<int>(P.map.h);   // <= SP_MAX_HIDDEN
+  constexpr int kChunk = 8 * NTHR;
+  const int nchunk = (h + kChunk - 1) / kChunk;
   const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
   const bool has_skip = P.has_skip != 0;
-  // one staged chunk ("item"): [dY | Z | skip (optional) | mask] of all threads
-  constexpr size_t v16 = static_cast<size_t>(NTHR) * 16;
-  const size_t off_mask = (has_skip ? 3 : 2) * v16;
-  const size_t item_bytes = off_mask + static_cast<size_t>(NTHR) * 8;
-  float2* red = reinterpret_cast<float2*>(smem + RING * MAXC * item_bytes);   // [2][32]
+  // one staged chunk ("item") of all threads: [dY | Z | mask | skip (optional)]
+  constexpr int v16 = NTHR * 16;
+  constexpr int off_mask = 2 * v16;
+  constexpr int off_skip = off_mask + NTHR * 8;
+  const int item_bytes = off_skip + (has_skip ? v16 : 0);
+  const int row_bytes = MAXC * item_bytes;
+  float2* red = reinterpret_cast<float2*>(smem + RING * row_bytes);   // [2][32]
+  const int c0 = tid * 8;
+  uint32_t valid = 0;   // bit ch: this thread has channels in chunk ch
+#pragma unroll
+  for (int ch = 0; ch < MAXC; ++ch)
+    if (ch < nchunk && ch * kChunk + c0 < h) valid |= 1u << ch;
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
@@ -47,14 +54,11 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   // gamma of this thread's channels, kept for every row
   uint4 gam[MAXC];
 #pragma unroll
-  for (int ch = 0; ch < MAXC; ++ch) {
-    const int64_t c = ch * kChunk + tid * 8;
-    gam[ch] = (ch < nchunk && c < h) ? ldg16(P.gamma + c) : make_uint4(0, 0, 0, 0);
-  }
+  for (int ch = 0; ch < MAXC; ++ch)
+    gam[ch] = ((valid >> ch) & 1u) ? ldg16(P.gamma + ch * kChunk + c0) : make_uint4(0, 0, 0, 0);
 
-  // Stage row ri (all of its chunks, one cp.async group) into ring slot
-  // ri % RING; rows are issued in order, so one cursor walks them.
-  const int64_t c0 = tid * 8;
+  // Stage the next row (all of its chunks, one cp.async group) into the next
+  // ring slot; rows are issued in order, so one cursor walks them.
   RowCursor pf;
   pf.init(P.map, blockIdx.x);
   int64_t pf_ri = 0;
@@ -63,16 +67,18 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
     if (pf_ri < nrows) {
       const int k = pf.k;
       const int64_t lo0 = pf.local(P.map) * h + c0;
-      uint8_t* base = smem + pf_slot * MAXC * static_cast<int>(item_bytes);
+      const uint16_t* dyp = P.dy[k] + lo0;
+      const uint16_t* zp = P.z[k] + lo0;
+      const uint8_t* mp = P.mask[k] + lo0;
+      uint8_t* it0 = smem + pf_slot * row_bytes + tid * 16;
 #pragma unroll
       for (int ch = 0; ch < MAXC; ++ch) {
-        if (ch < nchunk && ch * kChunk + c0 < h) {
-          uint8_t* it = base + ch * item_bytes;
-          const int64_t lo = lo0 + ch * kChunk;
-          cp_async16(it + tid * 16, P.dy[k] + lo);
-          cp_async16(it + v16 + tid * 16, P.z[k] + lo);
-          if (has_skip) cp_async16(it + 2 * v16 + tid * 16, P.dz_skip[k] + lo);
-          cp_async8(it + off_mask + tid * 8, P.mask[k] + lo);
+        if ((valid >> ch) & 1u) {
+          uint8_t* it = it0 + ch * item_bytes;
+          cp_async16(it, dyp + ch * kChunk);
+          cp_async16(it + v16, zp + ch * kChunk);
+          cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // mask slots: 8 B apart
+          if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
         }
       }
       if (++pf_ri < nrows) pf.advance(P.map, G);
@@ -120,68 +126,75 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
 
     issue_row();                    // row ri + RING - 1 refills the slot row ri - 1 used
     cp_async_wait<RING - 1>();      // row ri has landed
-    const uint8_t* base = smem + slot * MAXC * static_cast<int>(item_bytes) + tid * 16;
+    const uint8_t* it0 = smem + slot * row_bytes + tid * 16;
     slot = (slot + 1 == RING) ? 0 : slot + 1;
 
     // ---- pass 1: the two row sums, and dgamma / dbeta terms --------------
     // x_hat = (z - mean) * rstd (LN) or z * rstd (RMS); dxh = dY * gamma is an
     // exact product of two bf16 values
     const float nmean = is_ln ? -mean : 0.f;
-    float s1 = 0.f, s2 = 0.f;
+    float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
-      if (ch < nchunk && ch * kChunk + c0 < h) {
-        const uint8_t* it = base + ch * item_bytes;
+      if ((valid >> ch) & 1u) {
+        const uint8_t* it = it0 + ch * item_bytes;
         const uint4 dyv = lds16(it);
         const uint4 zv = lds16(it + v16);
         float xh[8], dxh[8], dy[8];
-        add8_bf16_bcast(zv, nmean, xh);
-        fma8_bf16_bcast(dyv, gam[ch], 0.f, dxh);
-        if (is_ln) add8_bf16(dyv, acc_b[ch]);
+        add8_bf16_bcast(zv, nmean, xh);             // z - mean
+        fma8_bf16_bcast(dyv, gam[ch], 0.f, dxh);    // dY * gamma
+        if (is_ln) add8_bf16(dyv, acc_b[ch]);       // dbeta terms
         unpack8(dyv, dy);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          xh[e] *= rstd;
-          s1 += dxh[e];
-          s2 = fmaf(dxh[e], xh[e], s2);
-          acc_g[ch][e] = fmaf(dy[e], xh[e], acc_g[ch][e]);
+        for (int e = 0; e < 8; e += 2) {
+          mul2(xh[e], xh[e + 1], rstd, rstd);
+          add2(s1a, s1b, dxh[e], dxh[e + 1]);
+          fma2(s2a, s2b, dxh[e], dxh[e + 1], xh[e], xh[e + 1]);
+          fma2(acc_g[ch][e], acc_g[ch][e + 1], dy[e], dy[e + 1], xh[e], xh[e + 1]);
         }
       }
     }
 
-    const float2 s = block_sum2(s1, s2, red + 32 * slot_sel);
+    const float2 s = block_sum2(s1a + s1b, s2a + s2b, red + 32 * slot_sel);
     slot_sel ^= 1;
     const float nm1 = is_ln ? -(s.x / fh) : 0.f;
-    const float m2r = (s.y / fh) * rstd;
+    const float nm2r = -(s.y / fh) * rstd;
 
     // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
     // dZ = rstd * (dxh - m1 - (z - mean) * rstd * m2)
     uint16_t* dres_row = P.dresidual[k] + local * h + c0;
     const int64_t grow = row * h + c0;
+    uint16_t* dg0_row = P.n_gather > 0 ? P.dgathered[0] + grow : nullptr;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
-      const int cc = ch * static_cast<int>(kChunk);
-      if (ch < nchunk && cc + c0 < h) {
-        const uint8_t* it = base + ch * item_bytes;
+      if ((valid >> ch) & 1u) {
+        const uint8_t* it = it0 + ch * item_bytes;
         const uint4 dyv = lds16(it);
         const uint4 zv = lds16(it + v16);
-        const uint2 mk = lds8(it + off_mask - tid * 8);   // mask slots are 8 B apart
+        const uint2 mk = lds8(it + off_mask - tid * 8);
         float zc[8], dz[8], dp[8];
         add8_bf16_bcast(zv, nmean, zc);           // z - mean
         fma8_bf16_bcast(dyv, gam[ch], nm1, dz);  // dxh - m1
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dz[e] = rstd * fmaf(-zc[e], m2r, dz[e]);
-        if (has_skip) add8_bf16(lds16(it + 2 * v16), dz);
+        for (int e = 0; e < 8; e += 2) {
+          fma2(dz[e], dz[e + 1], zc[e], zc[e + 1], nm2r, nm2r);
+          mul2(dz[e], dz[e + 1], rstd, rstd);
+        }
+        if (has_skip) add8_bf16(lds16(it + off_skip), dz);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) mul2_to(dz[e], dz[e + 1], P.scale, dp[e], dp[e + 1]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           // mask bytes are 0 or 1: bit 0 of byte e decides
           const bool kept = ((e < 4 ? mk.x : mk.y) & (1u << (8 * (e & 3)))) != 0u;
-          dp[e] = kept ? dz[e] * P.scale : 0.f;
-          acc_bias[ch][e] += dp[e];
+          dp[e] = kept ? dp[e] : 0.f;
         }
-        st16_stream(dres_row + cc, pack8(dz));
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) add2(acc_bias[ch][e], acc_bias[ch][e + 1], dp[e], dp[e + 1]);
+        st16_stream(dres_row + ch * kChunk, pack8(dz));
         const uint4 pb = pack8(dp);
-        for (int j = 0; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + cc, pb);
+        if (dg0_row != nullptr) st16_stream(dg0_row + ch * kChunk, pb);
+        for (int j = 1; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
       }
     }
     cur_mean = nx_mean;
@@ -193,8 +206,8 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   float* wsb = P.ws + static_cast<int64_t>(blockIdx.x) * 3 * h;
 #pragma unroll
   for (int ch = 0; ch < MAXC; ++ch) {
-    const int64_t c = ch * kChunk + tid * 8;
-    if (ch < nchunk && c < h) {
+    const int c = ch * kChunk + c0;
+    if ((valid >> ch) & 1u) {
       float4* dg = reinterpret_cast<float4*>(wsb + c);
       float4* db = reinterpret_cast<float4*>(wsb + h + c);
       float4* dc = reinterpret_cast<float4*>(wsb + 2 * h + c);

@@ -124,8 +124,11 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
                                                    P.off1),
                                         P.key0, P.key1);
           const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          float ys[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = (u[e] >= P.thr) ? __fmul_rn(y[e], P.scale) : 0.f;
+          for (int e = 0; e < 8; e += 2) mul2_to(y[e], y[e + 1], P.scale, ys[e], ys[e + 1]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = (u[e] >= P.thr) ? ys[e] : 0.f;
           keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         }
         // (with p == 0 the scale is exactly 1 and y * 1 == y)
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
     if (is_ln) {
       mean = block_sum(lsum, red + 32 * slot_sel) / fh;
       slot_sel ^= 1;
-      float lsq = 0.f;
+      float lsqa = 0.f, lsqb = 0.f;
       const float nmean = -mean;
 #pragma unroll 1
       for (int ch = 0; ch < nchunk; ++ch) {
@@ -165,10 +168,10 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
           float d[8];
           add8_bf16_bcast(lds16(zbuf + ch * kStream), nmean, d);   // z - mean
 #pragma unroll
-          for (int e = 0; e < 8; ++e) lsq = fmaf(d[e], d[e], lsq);
+          for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
         }
       }
-      const float var = block_sum(lsq, red + 32 * slot_sel) / fh;
+      const float var = block_sum(lsqa + lsqb, red + 32 * slot_sel) / fh;
       slot_sel ^= 1;
       rstd = rsqrtf(var + P.eps);
     } else {
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
 
     // ---- normalise and write into the all-gather destination(s) ----------
     const int64_t orow = row * h + c0;
+    uint16_t* g0_row = P.n_gather > 0 ? P.gathered[0] + orow : nullptr;
 #pragma unroll 1
     for (int ch = 0; ch < nchunk; ++ch) {
       const int cc = ch * kChunk;
@@ -192,14 +196,20 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
           unpack8(ldg16(P.beta + cc + c0), bt);
           add8_bf16_bcast(zv, -mean, o);   // z - mean
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = fmaf(o[e] * rstd, g[e], bt[e]);
+          for (int e = 0; e < 8; e += 2) {
+            mul2(o[e], o[e + 1], rstd, rstd);
+            fma2(bt[e], bt[e + 1], o[e], o[e + 1], g[e], g[e + 1]);   // * gamma + beta
+            o[e] = bt[e];
+            o[e + 1] = bt[e + 1];
+          }
         } else {
           fma8_bf16_bcast(zv, gv, 0.f, o);   // z * gamma, exact
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] *= rstd;
+          for (int e = 0; e < 8; e += 2) mul2(o[e], o[e + 1], rstd, rstd);
         }
         const uint4 ob = pack8(o);
-        for (int j = 0; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
+        if (g0_row != nullptr) st16_stream(g0_row + cc, ob);
+        for (int j = 1; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
       }
     }
     if (tid == 0) {

@@ -147,6 +147,54 @@ __device__ __forceinline__ void fma8_bf16(const uint4 a, const uint4 b, float c[
   fma2_bf16(a.w, b.w, c[6], c[7]);
 }
 
+// ------------------------------------------------- packed fp32 (f32x2) --
+// sm_100-class packed fp32 arithmetic: two independent IEEE fp32 operations
+// (round to nearest even, no fusion beyond what is written) in one
+// instruction.
+__device__ __forceinline__ void mul2(float& a0, float& a1, float b0, float b1) {
+  asm("{.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "mul.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// d = a * b + d, per lane, one rounding
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 d, {%0, %1};\n\t"
+      "fma.rn.f32x2 d, a, b, d;\n\t"
+      "mov.b64 {%0, %1}, d;}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// (d0, d1) = (a0 * b, a1 * b)
+__device__ __forceinline__ void mul2_to(float a0, float a1, float b, float& d0, float& d1) {
+  asm("{.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\t"
+      "mov.b64 {%0, %1}, d;}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b));
+}
+
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{.reg .b64 a, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 d, {%0, %1};\n\t"
+      "add.rn.f32x2 d, d, a;\n\t"
+      "mov.b64 {%0, %1}, d;}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 // Keep flags (0/1) of 4 draws against thr, and their 4 mask bytes.
 __device__ __forceinline__ uint32_t keep_bytes4(uint4 u, uint32_t thr) {
   const uint32_t k0 = u.x >= thr, k1 = u.y >= thr, k2 = u.z >= thr, k3 = u.w >= thr;
