@@ -18,8 +18,8 @@
 // channels in every row, it accumulates its channels' parameter-gradient
 // terms in registers across all rows of its block and writes one float32
 // partial per block and channel at the end; a second kernel sums the
-// partials over blocks in a fixed order (float64), so results are
-// bit-reproducible without atomics.
+// partials over blocks in a fixed order (eight float32 warp sums, combined in
+// float64), so results are bit-reproducible without atomics.
 #include "sp_device.cuh"
 
 namespace spb {
@@ -221,17 +221,46 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   }
 }
 
-// out[q][c] = sum over blocks (in block order, float64) of ws[block][q][c].
-__global__ void __launch_bounds__(256) param_reduce_kernel(const ParamReduceParams P) {
+// out[q][c] = sum over blocks b of ws[b][q][c], in a fixed order.  A block
+// owns 32 consecutive columns of one quantity q; warp w sums the partials
+// b = w, w + 8, w + 16, ... of its lane's column (float32, in that order;
+// each warp row is one coalesced 128-byte read) and the 8 warp sums are then
+// added in warp order in float64.  Same inputs, same bits.
+constexpr int kReduceWarps = 8;
+
+__global__ void __launch_bounds__(32 * kReduceWarps) param_reduce_kernel(const ParamReduceParams P) {
+  __shared__ float part[kReduceWarps][32];
   const int q = blockIdx.y;
   float* out = P.out[q];
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (out == nullptr || c >= P.h) return;
-  double acc = 0.0;
-  const float* src = P.ws + q * P.h + c;
+  if (out == nullptr) return;   // uniform per block
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   const int64_t stride = 3 * P.h;
-  for (int b = 0; b < P.nblk; ++b) acc += static_cast<double>(src[b * stride]);
-  out[c] = static_cast<float>(acc);
+  float acc = 0.f;
+  if (c < P.h) {
+    const float* src = P.ws + q * P.h + c;
+    int b = warp;
+    // four independent loads in flight per step
+    for (; b + 3 * kReduceWarps < P.nblk; b += 4 * kReduceWarps) {
+      const float v0 = src[b * stride];
+      const float v1 = src[(b + kReduceWarps) * stride];
+      const float v2 = src[(b + 2 * kReduceWarps) * stride];
+      const float v3 = src[(b + 3 * kReduceWarps) * stride];
+      acc += v0;
+      acc += v1;
+      acc += v2;
+      acc += v3;
+    }
+    for (; b < P.nblk; b += kReduceWarps) acc += src[b * stride];
+  }
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && c < P.h) {
+    double sum = 0.0;
+#pragma unroll
+    for (int w = 0; w < kReduceWarps; ++w) sum += static_cast<double>(part[w][lane]);
+    out[c] = static_cast<float>(sum);
+  }
 }
 
 template <int NTHR, int MAXC>
@@ -259,8 +288,8 @@ const void* bwd_kernel(int threads, int maxc, int ring) {
 }
 
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>((p.h + 255) / 256), 3);
-  param_reduce_kernel<<<grid, 256, 0, st>>>(p);
+  const dim3 grid(static_cast<unsigned>((p.h + 31) / 32), 3);
+  param_reduce_kernel<<<grid, 32 * kReduceWarps, 0, st>>>(p);
   return cudaGetLastError();
 }
 
