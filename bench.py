@@ -46,6 +46,15 @@ def fwd_bytes_per_token(t, h, n_gather, norm="layernorm"):
     return 2 * t * h + 2 * h + 2 * h + h + 2 * h * n_gather + stats
 
 
+def unfused_fwd_bytes_per_token(t, h, n_gather, norm="layernorm"):
+    """The unfused forward: reduce-scatter (t partials in, bf16 shard out), the
+    norm on the shard (shard, residual in; Z, mask, O, stats out), all-gather
+    (O in, n_gather copies out)."""
+    stats = 8 if norm == "layernorm" else 4
+    return (2 * t * h + 2 * h) + (2 * h + 2 * h + 2 * h + h + 2 * h + stats) \
+        + (2 * h + 2 * h * n_gather)
+
+
 def bwd_bytes_per_token(h, n_gather, norm="layernorm", skip=False):
     """Algorithmic bytes: dY, Z, mask, stats (+skip) read; dResidual, dYpre copies written."""
     stats = 8 if norm == "layernorm" else 4
@@ -200,9 +209,15 @@ def profiled_traffic():
 
 
 class Step:
-    """Device buffers and the fwd + bwd calls of one step."""
+    """Device buffers and the fwd + bwd calls of one step.
 
-    def __init__(self, w, device, n_gather=1):
+    pipeline "fused": one forward kernel; "unfused": reduce-scatter, norm on
+    the shards, all-gather as three calls (the ablation of the fusion).
+    """
+
+    def __init__(self, w, device, n_gather=1, pipeline="fused", mask="stored"):
+        self.pipeline = pipeline
+        self.mask_mode = mask
         from sp_boundary_norm_gb300 import binding as sp
         self.sp, self.w, self.dev = sp, w, device
         self.inp = wl.forward_inputs(w, device)
@@ -219,9 +234,22 @@ class Step:
         self.dgamma, self.dbeta, self.dbias = (e((w.h,), torch.float32) for _ in range(3))
         self.ws = e((sp.sp_norm_bwd_workspace_bytes(w.b, w.s, w.h, w.t),), torch.uint8)
         self.cu = (torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(device) if w.ragged else None)
+        if pipeline == "unfused":
+            self.y = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+            self.o = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
 
     def fwd(self):
         w, i = self.w, self.inp
+        if self.pipeline == "unfused":
+            self.sp.sp_reduce_scatter_seq(i["partials"], self.y, cu_seqlens=self.cu)
+            self.sp.sp_shard_norm_fwd(self.y, i["residual"], i["bias"], i["gamma"], i["beta"],
+                                      s=w.s, eps=w.eps, p=w.p, seed=w.seed, offset=w.offset,
+                                      norm=w.norm, cu_seqlens=self.cu, z_out=self.z,
+                                      mask_out=self.mask, mean_out=self.mean,
+                                      rstd_out=self.rstd, o_shards=self.o)
+            if self.gathered:
+                self.sp.sp_allgather_seq(self.o, self.gathered, s=w.s, cu_seqlens=self.cu)
+            return
         self.sp.sp_rs_norm_fwd(i["partials"], i["residual"], i["bias"], i["gamma"], i["beta"],
                                eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
                                cu_seqlens=self.cu, z_out=self.z, mask_out=self.mask, mean_out=self.mean,
@@ -229,6 +257,13 @@ class Step:
 
     def bwd(self):
         w = self.w
+        if self.mask_mode == "regen":
+            self.sp.sp_norm_bwd_philox(
+                self.dy, self.z, self.mean, self.rstd, self.inp["gamma"], None, s=w.s, p=w.p,
+                seed=w.seed, offset=w.offset, norm=w.norm, cu_seqlens=self.cu,
+                dresidual=self.dres, dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
+                dbias=self.dbias, workspace=self.ws)
+            return
         self.sp.sp_norm_bwd(self.dy, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"],
                             None, s=w.s, p=w.p, norm=w.norm, cu_seqlens=self.cu,
                             dresidual=self.dres,
@@ -341,7 +376,7 @@ def run_ours(args):
     if args.norm is not None:
         w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
                     name=f"{w.name}-{args.norm}")
-    step = Step(w, device, n_gather=args.n_gather)
+    step = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask)
     total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world, device)
     rejected = False
     if clocks_rejected(clocks):
@@ -351,8 +386,11 @@ def run_ours(args):
     total_ms = max_over_ranks(total_ms, world, device)
     tokens = w.tokens * args.steps * world
     value = tokens / (total_ms / 1e3)
-    fb = fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) * w.tokens
-    bb = bwd_bytes_per_token(w.h, args.n_gather, w.norm) * w.tokens
+    fused = args.pipeline == "fused"
+    fb = (fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
+          unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm)) * w.tokens
+    bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm)
+          - (w.h if args.mask == "regen" else 0)) * w.tokens
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     peak, peak_kind = measured_peak()
@@ -374,7 +412,8 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: LayerNorm boundary fwd+bwd, t={w.t} emulated ranks, "
                                f"b={w.b}, s={w.s}, h={w.h}, p={w.p}, n_gather={args.n_gather}",
                    "t": w.t, "b": w.b, "s": w.s, "h": w.h, "norm": w.norm, "p": w.p,
-                   "n_gather": args.n_gather,
+                   "n_gather": args.n_gather, "pipeline": args.pipeline,
+                   "backward_mask": args.mask,
                    "l2": "inputs larger than L2 (2.1 GB of partials per step), no flush",
                    "parallelism": f"replicas x{world} (independent batches)"},
         "hbm_gbs": round((fb + bb) / (step_ms / 1e3) / 1e9, 1),
@@ -383,13 +422,16 @@ def run_ours(args):
                 "bytes": fb, "tokens_per_s": round(w.tokens / (fwd_avg / 1e3), 1)},
         "bwd": {"ms": round(bwd_avg, 4), "gbs": round(bb / (bwd_avg / 1e3) / 1e9, 1),
                 "bytes": bb, "tokens_per_s": round(w.tokens / (bwd_avg / 1e3), 1)},
-        "roofline": {"bound": "hbm", "kernel": "rs_norm_fwd_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": "rs_norm_fwd_kernel" if fused else
+                               "unfused forward (reduce_scatter + shard norm + allgather)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": profiled_traffic(), "algorithmic_bytes": fb},
+                     "traffic": profiled_traffic() if fused else None,
+                     "algorithmic_bytes": fb},
         "e2e": {"value": round(w.tokens * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (3 if fused else 4 + (1 if args.n_gather else 0)) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -470,6 +512,10 @@ def parse_args(argv=None):
     ap.add_argument("--norm", choices=["layernorm", "rmsnorm"], default=None,
                     help="override the norm")
     ap.add_argument("--n-gather", type=int, default=1)
+    ap.add_argument("--mask", choices=["stored", "regen"], default="stored",
+                    help="regen: the backward draws the dropout mask again (mask-free)")
+    ap.add_argument("--pipeline", choices=["fused", "unfused"], default="fused",
+                    help="unfused: reduce-scatter, shard norm and all-gather as three calls")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -128,6 +128,32 @@ sp_status_t sp_allgather_seq(const void* const* shards, int64_t b, int64_t s, in
                              int32_t* dev_status, void* stream);
 
 /*
+ * sp_shard_norm_fwd -- the middle step of the unfused boundary: bias,
+ * dropout, residual-add and LayerNorm/RMSNorm on shards that were already
+ * reduced by a separate reduce-scatter (sp_reduce_scatter_seq, whose bf16
+ * output is the input here), writing O per shard for a separate all-gather
+ * (sp_allgather_seq).  The three calls together are the boundary without
+ * fusion (L7 §3.A applied step by step); they exist to measure what fusing
+ * them into sp_rs_norm_fwd saves.  Per token the arithmetic is that of
+ * sp_rs_norm_fwd with Y = the bf16 shard value (no rank sum); dropout draws
+ * use the token's index in the full sequence, so the mask equals the fused
+ * one.
+ *
+ * y_shards  [t]  (b, s_k, h) bf16  reduced partial sums of shard k (input)
+ * residual, bias, gamma, beta, eps, p, seed, offset, cu_seqlens, norm,
+ * z_out, mask_out, mean_out, rstd_out: as for sp_rs_norm_fwd
+ * o_shards  [t]  (b, s_k, h) bf16  normalised shard (output)
+ */
+sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* residual,
+                              const void* bias, const void* gamma, const void* beta,
+                              int64_t b, int64_t s, int64_t h, int32_t t, float eps, double p,
+                              uint64_t seed, uint64_t offset, const int32_t* cu_seqlens,
+                              int32_t n_seqs, sp_norm_t norm, void* const* z_out,
+                              uint8_t* const* mask_out, float* const* mean_out,
+                              float* const* rstd_out, void* const* o_shards,
+                              int32_t* dev_status, void* stream);
+
+/*
  * sp_reduce_scatter_seq -- g* alone, unfused: shards[k] = bf16_rne(sum over r
  * of partials[r] restricted to shard k), float32 sum in ascending r
  * (L7 §3.A, "前向转出 TP 区域").  In the backward it is the transpose of g
@@ -225,6 +251,26 @@ sp_status_t sp_norm_bwd_noalloc(const void* const* dy, const void* const* z,
                                 int32_t n_seqs, sp_norm_t norm, void* const* dresidual,
                                 void* const* dgathered, int32_t n_gather, float* dgamma,
                                 float* dbeta, float* dbias, int32_t* dev_status, void* stream);
+
+/*
+ * sp_norm_bwd_philox -- the mask-free backward: sp_norm_bwd with the dropout
+ * keep decisions drawn again from Philox4x32-10 instead of read from the
+ * stored 1-byte mask.  Because the forward's generator is counter-based and
+ * keyed on the element's global index (L7 answer to Q1: one seed on every
+ * rank), the same (seed, offset, p) reproduce the forward's mask exactly; the
+ * backward then reads h bytes less per token.  Arguments as for sp_norm_bwd,
+ * minus `mask`, plus the forward's `seed` and `offset`; the workspace size is
+ * sp_norm_bwd_workspace_bytes.
+ */
+sp_status_t sp_norm_bwd_philox(const void* const* dy, const void* const* z,
+                               const float* const* mean, const float* const* rstd,
+                               const void* gamma, const void* const* dz_skip, int64_t b,
+                               int64_t s, int64_t h, int32_t t, double p, uint64_t seed,
+                               uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
+                               sp_norm_t norm, void* const* dresidual, void* const* dgathered,
+                               int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               void* stream);
 
 /* Thread-local text of the last non-OK status returned on this thread. */
 const char* sp_last_error(void);

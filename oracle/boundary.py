@@ -191,6 +191,50 @@ def rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed,
     return res
 
 
+def shard_norm_fwd(y_shards, residual, bias, gamma, beta, *, s, eps, p, seed, offset=0,
+                   norm=LAYERNORM):
+    """Steps 2-5 on already reduced shards (the unfused boundary's middle step).
+
+    y_shards: t arrays (b, s_k, h) holding each rank's reduce-scatter output
+    as the collective delivered it (bf16 values).  Token indices, and hence
+    dropout draws, are those of the full sequence.  Returns per-shard lists
+    z, mask, mean, rstd, out (O of the shard) and out_exact.
+    """
+    t = len(y_shards)
+    b = np.asarray(y_shards[0]).shape[0]
+    h = np.asarray(y_shards[0]).shape[-1]
+    offs = _coll.shard_offsets(s, t)
+    res = {"z": [], "mask": [], "mean": [], "rstd": [], "out": [], "out_exact": []}
+    for k in range(t):
+        sk = offs[k + 1] - offs[k]
+        tok = (np.arange(b)[:, None] * s + offs[k] + np.arange(sk)[None, :]).reshape(-1)
+        one = _after_reduce(np.asarray(y_shards[k], dtype=np.float32).reshape(b * sk, h),
+                            np.asarray(residual[k]).reshape(b * sk, h), tok, bias, gamma, beta,
+                            eps=eps, p=p, seed=seed, offset=offset, norm=norm, exact=False)
+        for key in ("z", "mask", "out", "out_exact"):
+            res[key].append(one[key].reshape(b, sk, h))
+        res["mean"].append(None if one["mean"] is None else one["mean"].reshape(b, sk))
+        res["rstd"].append(one["rstd"].reshape(b, sk))
+    return res
+
+
+def unfused_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offset=0,
+                norm=LAYERNORM, n_gather=1):
+    """The boundary as three separate steps: a bf16 reduce-scatter (the float32
+    rank-ascending sum rounded to bf16, as a bf16 collective delivers it), the
+    token-wise ops on each shard, then the all-gather of the shards' O."""
+    shards_y, rs_bytes = _coll.reduce_scatter_seq(partials)
+    y16 = [_bf16.bf16_round(y) for y in shards_y]
+    s = np.asarray(partials[0]).shape[1]
+    res = shard_norm_fwd(y16, residual, bias, gamma, beta, s=s, eps=eps, p=p, seed=seed,
+                         offset=offset, norm=norm)
+    res["y_shards"] = y16
+    res["gathered"], res["ag_remote_bytes"] = (_coll.all_gather_seq(res["out"], n_gather)
+                                               if n_gather > 0 else ([], []))
+    res["rs_remote_bytes"] = rs_bytes
+    return res
+
+
 def unsharded_fwd(partials, residual_full, bias, gamma, beta, *, eps, p, seed,
                   offset=0, norm=LAYERNORM):
     """TP-only reference: all-reduce, then the token-wise ops on all tokens.

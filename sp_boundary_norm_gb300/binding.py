@@ -61,6 +61,14 @@ def load():
     lib.sp_norm_bwd.argtypes = [
         _PP, _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _vp, _i32,
         _i32, _PP, _PP, _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+    lib.sp_shard_norm_fwd.restype = _i32
+    lib.sp_shard_norm_fwd.argtypes = [
+        _PP, _PP, _vp, _vp, _vp, _i64, _i64, _i64, _i32, ctypes.c_float, ctypes.c_double,
+        _u64, _u64, _vp, _i32, _i32, _PP, _PP, _PP, _PP, _PP, _vp, _vp]
+    lib.sp_norm_bwd_philox.restype = _i32
+    lib.sp_norm_bwd_philox.argtypes = [
+        _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _u64, _u64, _vp,
+        _i32, _i32, _PP, _PP, _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
     lib.sp_norm_bwd_noalloc.restype = _i32
     lib.sp_norm_bwd_noalloc.argtypes = [
         _PP, _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _vp, _i32,
@@ -190,6 +198,39 @@ def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offse
     _check(code)
 
 
+def sp_shard_norm_fwd(y_shards, residual, bias, gamma, beta, *, s, eps, p, seed, offset=0,
+                      cu_seqlens=None, norm="layernorm", z_out, mask_out, mean_out, rstd_out,
+                      o_shards, status=None):
+    """Unfused middle step: bias + dropout + residual + norm on reduced shards."""
+    lib = load()
+    t = len(y_shards)
+    b, _, h = y_shards[0].shape
+    dev = y_shards[0].device
+    bf = torch.bfloat16
+    sizes = shard_sizes(s, t)
+    ln = norm == "layernorm"
+    for k in range(t):
+        for name, x in (("y_shards", y_shards), ("residual", residual), ("z_out", z_out),
+                        ("o_shards", o_shards)):
+            _need(x[k], (b, sizes[k], h), bf, dev, f"{name}[{k}]")
+        _need(mask_out[k], (b, sizes[k], h), torch.uint8, dev, f"mask_out[{k}]")
+        _need(rstd_out[k], (b, sizes[k]), torch.float32, dev, f"rstd_out[{k}]")
+        if ln:
+            _need(mean_out[k], (b, sizes[k]), torch.float32, dev, f"mean_out[{k}]")
+    for name, v in (("bias", bias), ("gamma", gamma)):
+        _need(v, (h,), bf, dev, name)
+    if ln:
+        _need(beta, (h,), bf, dev, "beta")
+    cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
+    st = device_status(dev) if status is None else status
+    _check(lib.sp_shard_norm_fwd(
+        _ptr_array(y_shards), _ptr_array(residual), _ptr(bias), _ptr(gamma),
+        _ptr(beta) if ln else None, b, s, h, t, float(eps), float(p), int(seed), int(offset),
+        cu, n_seqs, NORMS[norm], _ptr_array(z_out), _ptr_array(mask_out),
+        _ptr_array(mean_out) if ln else None, _ptr_array(rstd_out), _ptr_array(o_shards),
+        _ptr(st), _stream(dev)))
+
+
 def sp_allgather_seq(shards, gathered, *, s, cu_seqlens=None, status=None):
     """g alone: gathered[j][:, o_k:o_{k+1}, :] = shards[k] for every j."""
     lib = load()
@@ -265,6 +306,44 @@ def sp_norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlen
         _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev))
     _check(code)
+
+
+def sp_norm_bwd_philox(dy, z, mean, rstd, gamma, dz_skip=None, *, s, p, seed, offset=0,
+                       cu_seqlens=None, norm="layernorm", dresidual, dgathered, dgamma=None,
+                       dbeta=None, dbias=None, workspace, status=None):
+    """Mask-free backward: the dropout mask is drawn again from (seed, offset, p)."""
+    lib = load()
+    t = len(dy)
+    b, _, h = dy[0].shape
+    dev = dy[0].device
+    bf = torch.bfloat16
+    sizes = shard_sizes(s, t)
+    ln = norm == "layernorm"
+    for k in range(t):
+        _need(dy[k], (b, sizes[k], h), bf, dev, f"dy[{k}]")
+        _need(z[k], (b, sizes[k], h), bf, dev, f"z[{k}]")
+        _need(rstd[k], (b, sizes[k]), torch.float32, dev, f"rstd[{k}]")
+        if ln:
+            _need(mean[k], (b, sizes[k]), torch.float32, dev, f"mean[{k}]")
+        if dz_skip is not None:
+            _need(dz_skip[k], (b, sizes[k], h), bf, dev, f"dz_skip[{k}]")
+        _need(dresidual[k], (b, sizes[k], h), bf, dev, f"dresidual[{k}]")
+    for j, g in enumerate(dgathered):
+        _need(g, (b, s, h), bf, dev, f"dgathered[{j}]")
+    _need(gamma, (h,), bf, dev, "gamma")
+    for name, v in (("dgamma", dgamma), ("dbeta", dbeta), ("dbias", dbias)):
+        if v is not None:
+            _need(v, (h,), torch.float32, dev, name)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
+    st = device_status(dev) if status is None else status
+    _check(lib.sp_norm_bwd_philox(
+        _ptr_array(dy), _ptr_array(z), _ptr_array(mean) if ln else None, _ptr_array(rstd),
+        _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), int(seed), int(offset), cu,
+        n_seqs, NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
+        _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev)))
 
 
 NOALLOC_WORKSPACE_BYTES = 16 << 20

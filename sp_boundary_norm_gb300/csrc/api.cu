@@ -206,8 +206,20 @@ LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
                     [&](int st) { return fwd_kernel(threads, t, st); });
 }
 
-// Backward: a ring of whole rows (dY, Z, mask, optional skip gradient).
-LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip) {
+// The shard-input variant of the forward: two streams per stage.
+LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
+  const int threads = (h / 8 <= 64) ? 64 : 256;
+  const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
+  const size_t stage = static_cast<size_t>(2) * threads * 16;
+  const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float);
+  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 3,
+                    /*stages=*/4, /*blocks per SM=*/threads == 64 ? 4 : 2,
+                    [&](int st) { return fwd_shard_kernel(threads, st); });
+}
+
+// Backward: a ring of whole rows (dY, Z, mask unless regenerated, optional
+// skip gradient).
+LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
   const int64_t nvec = h / 8;
   int threads, maxc;
   if (nvec <= 64) {
@@ -220,11 +232,14 @@ LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip) {
     threads = 512;
     maxc = pow2_at_least(static_cast<int>((nvec + 511) / 512));
   }
-  const size_t item = static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + threads * 8;
+  const size_t item =
+      static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
   const size_t ring_row = item * maxc;
   return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 3,
-                    /*ring=*/2, /*blocks per SM=*/threads == 512 ? 1 : 2,
-                    [&](int st) { return bwd_kernel(threads, maxc, st); });
+                    /*ring=*/2, /*blocks per SM=*/threads == 512 ? 1 : 2, [&](int st) {
+                      return regen ? bwd_regen_kernel(threads, maxc, st)
+                                   : bwd_kernel(threads, maxc, st);
+                    });
 }
 
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
@@ -358,6 +373,86 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   return SP_OK;
 }
 
+sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* residual,
+                              const void* bias, const void* gamma, const void* beta, int64_t b,
+                              int64_t s, int64_t h, int32_t t, float eps, double p,
+                              uint64_t seed, uint64_t offset, const int32_t* cu_seqlens,
+                              int32_t n_seqs, sp_norm_t norm, void* const* z_out,
+                              uint8_t* const* mask_out, float* const* mean_out,
+                              float* const* rstd_out, void* const* o_shards,
+                              int32_t* dev_status, void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
+  if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
+    return fail(SP_ERR_INVALID_ARG, "unknown norm %d", (int)norm);
+  if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SP_ERR_INVALID_ARG, "eps must be > 0");
+  if (!(p >= 0.0 && p < 1.0)) return fail(SP_ERR_INVALID_ARG, "p = %g outside [0, 1)", p);
+  const bool ln = norm == SP_NORM_LAYERNORM;
+  if (b * s == 0) return SP_OK;
+  const ShardMap map = make_map(b, s, h, t);
+  if ((st = check_ptrs(y_shards, t, "y_shards", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(residual, t, "residual", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(z_out, t, "z_out", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(rstd_out, t, "rstd_out", false, &map)) != SP_OK) return st;
+  if (ln && (st = check_ptrs(mean_out, t, "mean_out", false, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(o_shards, t, "o_shards", true, &map)) != SP_OK) return st;
+  if ((st = check_vec(bias, "bias")) != SP_OK) return st;
+  if ((st = check_vec(gamma, "gamma")) != SP_OK) return st;
+  if (ln && (st = check_vec(beta, "beta")) != SP_OK) return st;
+  if (dev_status != nullptr && (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
+  Ranges rg;
+  for (int k = 0; k < t; ++k) {
+    const size_t n = static_cast<size_t>(shard_rows(map, k));
+    rg.add(y_shards[k], n * h * 2, false, "y_shards", k);
+    rg.add(residual[k], n * h * 2, false, "residual", k);
+    rg.add(z_out[k], n * h * 2, true, "z_out", k);
+    rg.add(mask_out[k], n * h, true, "mask_out", k);
+    rg.add(rstd_out[k], n * 4, true, "rstd_out", k);
+    if (ln) rg.add(mean_out[k], n * 4, true, "mean_out", k);
+    rg.add(o_shards[k], n * h * 2, true, "o_shards", k);
+  }
+  rg.add(bias, h * 2, false, "bias", 0);
+  rg.add(gamma, h * 2, false, "gamma", 0);
+  if (ln) rg.add(beta, h * 2, false, "beta", 0);
+  if ((st = rg.check()) != SP_OK) return st;
+
+  FwdParams P{};
+  P.map = map;
+  for (int k = 0; k < t; ++k) {
+    P.partials[k] = static_cast<const uint16_t*>(y_shards[k]);
+    P.residual[k] = static_cast<const uint16_t*>(residual[k]);
+    P.z[k] = static_cast<uint16_t*>(z_out[k]);
+    P.mask[k] = mask_out[k];
+    P.rstd[k] = rstd_out[k];
+    P.mean[k] = ln ? mean_out[k] : nullptr;
+    P.gathered[k] = static_cast<uint16_t*>(o_shards[k]);
+  }
+  P.bias = static_cast<const uint16_t*>(bias);
+  P.gamma = static_cast<const uint16_t*>(gamma);
+  P.beta = ln ? static_cast<const uint16_t*>(beta) : nullptr;
+  P.cu_seqlens = cu_seqlens;
+  P.n_seqs = n_seqs;
+  P.n_gather = t;
+  P.norm = norm;
+  P.thr = static_cast<uint32_t>(std::floor(p * 4294967296.0));
+  P.scale = static_cast<float>(1.0 / (1.0 - p));
+  P.eps = eps;
+  P.key0 = static_cast<uint32_t>(seed);
+  P.key1 = static_cast<uint32_t>(seed >> 32);
+  P.off0 = static_cast<uint32_t>(offset);
+  P.off1 = static_cast<uint32_t>(offset >> 32);
+  P.rows = b * s;
+  P.status = dev_status;
+  const LaunchShape ls = fwd_shard_shape(P.rows, h);
+  const cudaError_t e = launch(fwd_shard_kernel(ls.threads, ls.stages), ls, &P,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "sp_shard_norm_fwd launch");
+  return SP_OK;
+}
+
 static sp_status_t seq_copy_common(const void* const* src, int n_src, const char* src_name,
                                    bool src_full, void* const* dst, int n_dst,
                                    const char* dst_name, bool dst_full, int64_t b, int64_t s,
@@ -427,22 +522,25 @@ size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, s
   (void)norm;
   if (b <= 0 || s <= 0 || h < 8 || h % 8 != 0 || h > SP_MAX_HIDDEN || t < 1 || t > SP_MAX_RANKS)
     return 0;
-  // the skip gradient does not change the grid (same threads and occupancy cap)
-  const LaunchShape ls = bwd_shape(b * s, h, false);
-  const LaunchShape ls2 = bwd_shape(b * s, h, true);
-  const int grid = ls.grid > ls2.grid ? ls.grid : ls2.grid;
+  // the largest grid over the variants (skip gradient or not, stored or
+  // regenerated mask): one workspace size serves every backward entry point
+  int grid = 0;
+  for (int v = 0; v < 4; ++v) {
+    const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v & 2) != 0);
+    if (ls.grid > grid) grid = ls.grid;
+  }
   return static_cast<size_t>(grid) * 3 * static_cast<size_t>(h) * sizeof(float);
 }
 
-sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8_t* const* mask,
-                        const float* const* mean, const float* const* rstd, const void* gamma,
-                        const void* const* dz_skip, int64_t b, int64_t s, int64_t h, int32_t t,
-                        double p, const int32_t* cu_seqlens, int32_t n_seqs, sp_norm_t norm,
-                        void* const* dresidual, void* const* dgathered, int32_t n_gather,
-                        float* dgamma, float* dbeta, float* dbias, void* workspace,
-                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+static sp_status_t norm_bwd_common(
+    const void* const* dy, const void* const* z, const uint8_t* const* mask,
+    const float* const* mean, const float* const* rstd, const void* gamma,
+    const void* const* dz_skip, int64_t b, int64_t s, int64_t h, int32_t t, double p,
+    bool regen, uint64_t seed, uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
+    sp_norm_t norm, void* const* dresidual, void* const* dgathered, int32_t n_gather,
+    float* dgamma, float* dbeta, float* dbias, void* workspace, size_t workspace_bytes,
+    int32_t* dev_status, void* stream) {
   sp_status_t st;
-  if (take_injected(&st)) return st;
   if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
   if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
     return fail(SP_ERR_INVALID_ARG, "unknown norm %d", (int)norm);
@@ -467,7 +565,7 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
   const ShardMap map = make_map(b, s, h, t);
   if ((st = check_ptrs(dy, t, "dy", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(z, t, "z", true, &map)) != SP_OK) return st;
-  if ((st = check_ptrs(mask, t, "mask", true, &map)) != SP_OK) return st;
+  if (!regen && (st = check_ptrs(mask, t, "mask", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(rstd, t, "rstd", false, &map)) != SP_OK) return st;
   if (ln && (st = check_ptrs(mean, t, "mean", false, &map)) != SP_OK) return st;
   if (dz_skip != nullptr && (st = check_ptrs(dz_skip, t, "dz_skip", true, &map)) != SP_OK)
@@ -479,7 +577,7 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
     return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
 
   const bool has_skip = dz_skip != nullptr;
-  const LaunchShape ls = bwd_shape(rows, h, has_skip);
+  const LaunchShape ls = bwd_shape(rows, h, has_skip, regen);
   const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SP_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need,
@@ -492,7 +590,7 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
     const size_t n = static_cast<size_t>(shard_rows(map, k));
     rg.add(dy[k], n * h * 2, false, "dy", k);
     rg.add(z[k], n * h * 2, false, "z", k);
-    rg.add(mask[k], n * h, false, "mask", k);
+    if (!regen) rg.add(mask[k], n * h, false, "mask", k);
     rg.add(rstd[k], n * 4, false, "rstd", k);
     if (ln) rg.add(mean[k], n * 4, false, "mean", k);
     if (has_skip) rg.add(dz_skip[k], n * h * 2, false, "dz_skip", k);
@@ -511,7 +609,7 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
   for (int k = 0; k < t; ++k) {
     P.dy[k] = static_cast<const uint16_t*>(dy[k]);
     P.z[k] = static_cast<const uint16_t*>(z[k]);
-    P.mask[k] = mask[k];
+    P.mask[k] = regen ? nullptr : mask[k];
     P.rstd[k] = rstd[k];
     P.mean[k] = ln ? mean[k] : nullptr;
     P.dz_skip[k] = has_skip ? static_cast<const uint16_t*>(dz_skip[k]) : nullptr;
@@ -525,12 +623,20 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
   P.norm = norm;
   P.has_skip = has_skip ? 1 : 0;
   P.scale = static_cast<float>(1.0 / (1.0 - p));
+  // same keep rule as the forward: keep iff draw >= floor(p * 2^32)
+  P.thr = static_cast<uint32_t>(std::floor(p * 4294967296.0));
+  P.key0 = static_cast<uint32_t>(seed);
+  P.key1 = static_cast<uint32_t>(seed >> 32);
+  P.off0 = static_cast<uint32_t>(offset);
+  P.off1 = static_cast<uint32_t>(offset >> 32);
   P.rows = rows;
   P.ws = static_cast<float*>(workspace);
   P.status = dev_status;
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch(bwd_kernel(ls.threads, ls.maxc, ls.stages), ls, &P, cs);
+  const void* fn = regen ? bwd_regen_kernel(ls.threads, ls.maxc, ls.stages)
+                         : bwd_kernel(ls.threads, ls.maxc, ls.stages);
+  cudaError_t e = launch(fn, ls, &P, cs);
   if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd launch");
   if (dgamma || (dbeta && ln) || dbias) {
     ParamReduceParams R{};
@@ -544,6 +650,36 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
     if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd parameter reduce launch");
   }
   return SP_OK;
+}
+
+sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8_t* const* mask,
+                        const float* const* mean, const float* const* rstd, const void* gamma,
+                        const void* const* dz_skip, int64_t b, int64_t s, int64_t h, int32_t t,
+                        double p, const int32_t* cu_seqlens, int32_t n_seqs, sp_norm_t norm,
+                        void* const* dresidual, void* const* dgathered, int32_t n_gather,
+                        float* dgamma, float* dbeta, float* dbias, void* workspace,
+                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  return norm_bwd_common(dy, z, mask, mean, rstd, gamma, dz_skip, b, s, h, t, p, false, 0, 0,
+                         cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma, dbeta,
+                         dbias, workspace, workspace_bytes, dev_status, stream);
+}
+
+sp_status_t sp_norm_bwd_philox(const void* const* dy, const void* const* z,
+                               const float* const* mean, const float* const* rstd,
+                               const void* gamma, const void* const* dz_skip, int64_t b,
+                               int64_t s, int64_t h, int32_t t, double p, uint64_t seed,
+                               uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
+                               sp_norm_t norm, void* const* dresidual, void* const* dgathered,
+                               int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  return norm_bwd_common(dy, z, nullptr, mean, rstd, gamma, dz_skip, b, s, h, t, p, true, seed,
+                         offset, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma,
+                         dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
 }
 
 const char* sp_last_error(void) { return g_err; }

@@ -24,7 +24,10 @@
 
 namespace spb {
 
-template <int NTHR, int MAXC, int RING>
+// REGEN = true: the mask-free variant; the dropout keep decisions are drawn
+// again from Philox4x32-10 at the element's global index (the forward's seed
+// and offset) instead of being read from the stored 1-byte mask.
+template <int NTHR, int MAXC, int RING, bool REGEN>
 __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -34,9 +37,10 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
   const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
   const bool has_skip = P.has_skip != 0;
   // one staged chunk ("item") of all threads: [dY | Z | mask | skip (optional)]
+  // (no mask slots in the mask-free variant)
   constexpr int v16 = NTHR * 16;
   constexpr int off_mask = 2 * v16;
-  constexpr int off_skip = off_mask + NTHR * 8;
+  constexpr int off_skip = off_mask + (REGEN ? 0 : NTHR * 8);
   const int item_bytes = off_skip + (has_skip ? v16 : 0);
   const int row_bytes = MAXC * item_bytes;
   float2* red = reinterpret_cast<float2*>(smem + RING * row_bytes);   // [2][32]
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
       const int64_t lo0 = pf.local(P.map) * h + c0;
       const uint16_t* dyp = P.dy[k] + lo0;
       const uint16_t* zp = P.z[k] + lo0;
-      const uint8_t* mp = P.mask[k] + lo0;
+      const uint8_t* mp = REGEN ? nullptr : P.mask[k] + lo0;
       uint8_t* it0 = smem + pf_slot * row_bytes + tid * 16;
 #pragma unroll
       for (int ch = 0; ch < MAXC; ++ch) {
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
           uint8_t* it = it0 + ch * item_bytes;
           cp_async16(it, dyp + ch * kChunk);
           cp_async16(it + v16, zp + ch * kChunk);
-          cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // mask slots: 8 B apart
+          if (!REGEN) cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // 8 B apart
           if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
         }
       }
@@ -171,7 +175,20 @@ __global__ void __launch_bounds__(NTHR, 1) norm_bwd_kernel(const BwdParams P) {
         const uint8_t* it = it0 + ch * item_bytes;
         const uint4 dyv = lds16(it);
         const uint4 zv = lds16(it + v16);
-        const uint2 mk = lds8(it + off_mask - tid * 8);
+        uint2 mk;
+        if (REGEN) {
+          const uint64_t q = static_cast<uint64_t>(grow + ch * kChunk) >> 2;
+          const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
+                                                   static_cast<uint32_t>(q >> 32), P.off0, P.off1),
+                                        P.key0, P.key1);
+          const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+                                                   static_cast<uint32_t>((q + 1) >> 32), P.off0,
+                                                   P.off1),
+                                        P.key0, P.key1);
+          mk = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
+        } else {
+          mk = lds8(it + off_mask - tid * 8);
+        }
         float zc[8], dz[8], dp[8];
         add8_bf16_bcast(zv, nmean, zc);           // z - mean
         fma8_bf16_bcast(dyv, gam[ch], nm1, dz);  // dxh - m1
@@ -263,12 +280,25 @@ __global__ void __launch_bounds__(32 * kReduceWarps) param_reduce_kernel(const P
   }
 }
 
-template <int NTHR, int MAXC>
+template <int NTHR, int MAXC, bool REGEN>
 static const void* bwd_kernel_s(int ring) {
   switch (ring) {
-    case 2: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 2>);
-    case 3: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 3>);
-    case 4: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 4>);
+    case 2: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 2, REGEN>);
+    case 3: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 3, REGEN>);
+    case 4: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 4, REGEN>);
+    default: return nullptr;
+  }
+}
+
+template <bool REGEN>
+static const void* bwd_kernel_any(int threads, int maxc, int ring) {
+  if (threads == 64) return maxc == 1 ? bwd_kernel_s<64, 1, REGEN>(ring) : nullptr;
+  if (threads == 256) return maxc == 1 ? bwd_kernel_s<256, 1, REGEN>(ring) : nullptr;
+  if (threads != 512) return nullptr;
+  switch (maxc) {
+    case 1: return bwd_kernel_s<512, 1, REGEN>(ring);
+    case 2: return bwd_kernel_s<512, 2, REGEN>(ring);
+    case 4: return bwd_kernel_s<512, 4, REGEN>(ring);
     default: return nullptr;
   }
 }
@@ -276,15 +306,11 @@ static const void* bwd_kernel_s(int ring) {
 // Instantiated shapes (threads, chunks per row): (64, 1) for h <= 512,
 // (256, 1) for h <= 2048, (512, 1 | 2 | 4) above; ring of 2, 3 or 4 rows.
 const void* bwd_kernel(int threads, int maxc, int ring) {
-  if (threads == 64) return maxc == 1 ? bwd_kernel_s<64, 1>(ring) : nullptr;
-  if (threads == 256) return maxc == 1 ? bwd_kernel_s<256, 1>(ring) : nullptr;
-  if (threads != 512) return nullptr;
-  switch (maxc) {
-    case 1: return bwd_kernel_s<512, 1>(ring);
-    case 2: return bwd_kernel_s<512, 2>(ring);
-    case 4: return bwd_kernel_s<512, 4>(ring);
-    default: return nullptr;
-  }
+  return bwd_kernel_any<false>(threads, maxc, ring);
+}
+
+const void* bwd_regen_kernel(int threads, int maxc, int ring) {
+  return bwd_kernel_any<true>(threads, maxc, ring);
 }
 
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st) {

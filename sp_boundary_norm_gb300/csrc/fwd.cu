@@ -23,12 +23,19 @@
 
 namespace spb {
 
-template <int NTHR, int STAGES, int TT>
+// SHARD = false: the fused boundary (inputs: the t full partials; output:
+// the gathered full buffers).  SHARD = true: the middle step of the unfused
+// boundary (input: each rank's already reduced shard, one stream; output: O
+// of each shard in its own buffer; P.partials / P.gathered hold per-shard
+// pointers).  Dropout draws use the token's index in the full sequence in
+// both cases.
+template <int NTHR, int STAGES, int TT, bool SHARD>
 __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
     rs_norm_fwd_kernel(const FwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
-  const int t = TT > 0 ? TT : P.map.t;     // compile-time rank count when specialised
+  // input streams summed per element (compile-time when specialised)
+  const int t = SHARD ? 1 : (TT > 0 ? TT : P.map.t);
   const int64_t h = P.map.h;
   constexpr int kChunk = 8 * NTHR;
   const int nchunk = static_cast<int>((h + kChunk - 1) / kChunk);
@@ -56,9 +63,13 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
     if (pf_ri < nrows) {
       if (pf_chunk * kChunk + c0 < h) {
         uint8_t* slot = smem + pf_stage * stage_bytes + tid * 16;
+        if (SHARD) {
+          cp_async16(slot, P.partials[pf.k] + pf_roff);
+        } else {
 #pragma unroll
-        for (int r = 0; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
-          if (TT > 0 || r < t) cp_async16(slot + r * kStream, P.partials[r] + pf_goff);
+          for (int r = 0; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
+            if (TT > 0 || r < t) cp_async16(slot + r * kStream, P.partials[r] + pf_goff);
+        }
         cp_async16(slot + t * kStream, P.residual[pf.k] + pf_roff);
       }
       if (++pf_chunk == nchunk) {
@@ -108,9 +119,11 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
         // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
         float y[8];
         unpack8(lds16(slot), y);
+        if (!SHARD) {
 #pragma unroll
-        for (int r = 1; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
-          if (TT > 0 || r < t) add8_bf16(lds16(slot + r * kStream), y);
+          for (int r = 1; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
+            if (TT > 0 || r < t) add8_bf16(lds16(slot + r * kStream), y);
+        }
         add8_bf16(bv, y);   // + bias
         // dropout: element e keeps iff its Philox word >= thr
         uint2 keep = make_uint2(0x01010101u, 0x01010101u);
@@ -182,7 +195,8 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
 
     // ---- normalise and write into the all-gather destination(s) ----------
     const int64_t orow = row * h + c0;
-    uint16_t* g0_row = P.n_gather > 0 ? P.gathered[0] + orow : nullptr;
+    uint16_t* g0_row = SHARD ? P.gathered[k] + local * h + c0
+                             : (P.n_gather > 0 ? P.gathered[0] + orow : nullptr);
 #pragma unroll 1
     for (int ch = 0; ch < nchunk; ++ch) {
       const int cc = ch * kChunk;
@@ -209,7 +223,8 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
         }
         const uint4 ob = pack8(o);
         if (g0_row != nullptr) st16_stream(g0_row + cc, ob);
-        for (int j = 1; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
+        if (!SHARD)
+          for (int j = 1; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
       }
     }
     if (tid == 0) {
@@ -220,12 +235,12 @@ __global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
   cp_async_wait<0>();
 }
 
-template <int NTHR, int TT>
+template <int NTHR, int TT, bool SHARD>
 static const void* fwd_kernel_s(int stages) {
   switch (stages) {
-    case 2: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 2, TT>);
-    case 3: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 3, TT>);
-    case 4: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 4, TT>);
+    case 2: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 2, TT, SHARD>);
+    case 3: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 3, TT, SHARD>);
+    case 4: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 4, TT, SHARD>);
     default: return nullptr;
   }
 }
@@ -234,8 +249,17 @@ static const void* fwd_kernel_s(int stages) {
 // or 4 chunks; t either a run-time value or the compile-time 8.
 const void* fwd_kernel(int threads, int t, int stages) {
   const bool t8 = (t == 8);
-  if (threads == 64) return t8 ? fwd_kernel_s<64, 8>(stages) : fwd_kernel_s<64, 0>(stages);
-  if (threads == 256) return t8 ? fwd_kernel_s<256, 8>(stages) : fwd_kernel_s<256, 0>(stages);
+  if (threads == 64)
+    return t8 ? fwd_kernel_s<64, 8, false>(stages) : fwd_kernel_s<64, 0, false>(stages);
+  if (threads == 256)
+    return t8 ? fwd_kernel_s<256, 8, false>(stages) : fwd_kernel_s<256, 0, false>(stages);
+  return nullptr;
+}
+
+// The shard-input / shard-output variant (one input stream).
+const void* fwd_shard_kernel(int threads, int stages) {
+  if (threads == 64) return fwd_kernel_s<64, 1, true>(stages);
+  if (threads == 256) return fwd_kernel_s<256, 1, true>(stages);
   return nullptr;
 }
 

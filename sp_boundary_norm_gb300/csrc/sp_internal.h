@@ -58,6 +58,9 @@ struct BwdParams {
   int32_t norm;
   int32_t has_skip;
   float scale;
+  uint32_t thr;          // mask regeneration (mask-free backward): keep iff draw >= thr
+  uint32_t key0, key1;   // Philox key = the forward's seed
+  uint32_t off0, off1;   // Philox counter offset = the forward's offset
   int64_t rows;
   float* ws;             // [gridDim.x][3][h] per-block parameter-gradient partials
   int32_t* status;
@@ -99,7 +102,9 @@ sp_status_t record_error(sp_status_t code, const char* message);
 // Forward: (threads, ranks t, pipeline stages); backward: (threads, chunks per
 // row, ring rows).
 const void* fwd_kernel(int threads, int t, int stages);
+const void* fwd_shard_kernel(int threads, int stages);
 const void* bwd_kernel(int threads, int maxc, int ring);
+const void* bwd_regen_kernel(int threads, int maxc, int ring);
 
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st);
 cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st);

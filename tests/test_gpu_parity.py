@@ -358,3 +358,102 @@ def test_device_philox_matches_oracle():
     zero_key = (words[:, 4] == 0) & (words[:, 5] == 0)
     for j in range(4):
         assert np.array_equal(got[zero_key, j], ref[j][zero_key])
+
+
+# ----------------------------------------------- unfused boundary (ablation)
+
+def _run_unfused(w, inp, n_gather=1):
+    sizes = w.shard_sizes()
+    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=C.DEV)
+    y = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+    out = C.alloc_fwd(w, n_gather)
+    o = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+    C.sp.sp_reduce_scatter_seq(inp["partials"], y)
+    C.sp.sp_shard_norm_fwd(y, inp["residual"], inp["bias"], inp["gamma"], inp["beta"], s=w.s,
+                           eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                           z_out=out["z"], mask_out=out["mask"], mean_out=out["mean"],
+                           rstd_out=out["rstd"], o_shards=o)
+    if n_gather:
+        C.sp.sp_allgather_seq(o, out["gathered"], s=w.s)
+    return y, o, out
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(t=3, s=48),
+                                     dict(b=2, s=40, t=4), dict(h=5120, s=32), dict(p=0.0)])
+def test_unfused_pipeline_matches_oracle(variant):
+    w = wl.Workload("uf", t=2, b=1, s=64, h=512, draw_seed=61).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    y, o, out = _run_unfused(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    ref = ob.unfused_fwd([C.f32(x) for x in inp["partials"]], [C.f32(x) for x in inp["residual"]],
+                         C.f32(inp["bias"]), C.f32(inp["gamma"]), C.f32(inp["beta"]), eps=w.eps,
+                         p=w.p, seed=w.seed, offset=w.offset, norm=w.norm, n_gather=1)
+    for k in range(w.t):
+        assert np.array_equal(compare.bf16_bits(y[k]), compare.bf16_bits(ref["y_shards"][k]))
+        assert np.array_equal(compare.bf16_bits(out["z"][k]), compare.bf16_bits(ref["z"][k]))
+        assert np.array_equal(out["mask"][k].cpu().numpy(), ref["mask"][k])
+        assert not compare.f32_rel_mismatch(out["rstd"][k].cpu().numpy(), ref["rstd"][k]).any()
+        mag = ob._norm_rows(ref["z"][k].reshape(-1, w.h).astype(np.float64), C.f32(inp["gamma"]),
+                            C.f32(inp["beta"]), w.eps, w.norm)[3].reshape(ref["z"][k].shape)
+        assert not compare.bf16_mismatch(compare.bf16_bits(o[k]), ref["out_exact"][k], mag).any()
+    full = np.concatenate(ref["out"], axis=1)
+    got = compare.bf16_bits(out["gathered"][0])
+    # the gathered copy is the shards' O laid out along s (bit-exact copy of o)
+    assert np.array_equal(got, np.concatenate([compare.bf16_bits(x) for x in o], axis=1))
+    assert got.shape == compare.bf16_bits(full).shape
+
+
+def test_unfused_mask_equals_fused_mask():
+    w = wl.Workload("ufm", t=4, b=1, s=128, h=1024, draw_seed=62)
+    inp = wl.forward_inputs(w, C.DEV)
+    _, _, un = _run_unfused(w, inp)
+    fu = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    for a, b in zip(un["mask"], fu["mask"]):
+        assert torch.equal(a, b)
+
+
+# ------------------------------------------------------ mask-free backward
+
+@pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(t=3, s=48),
+                                     dict(b=2, s=40, t=4), dict(p=0.0), dict(h=5120, s=24),
+                                     dict(seed=2**40 + 3, offset=2**33 + 1)])
+@pytest.mark.parametrize("with_skip", [False, True])
+def test_mask_free_backward_equals_stored_mask_backward(variant, with_skip):
+    w = wl.Workload("mf", t=2, b=1, s=64, h=512, draw_seed=71).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    bi = wl.backward_inputs(w, C.DEV, with_skip=with_skip)
+    ref = C.run_bwd(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], n_gather=1)
+    got = C.alloc_bwd(w, 1)
+    C.sp.sp_norm_bwd_philox(bi["dy"], fwd["z"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                            bi["dz_skip"], s=w.s, p=w.p, seed=w.seed, offset=w.offset,
+                            norm=w.norm, dresidual=got["dres"], dgathered=got["dgat"],
+                            dgamma=got["dgamma"],
+                            dbeta=got["dbeta"] if w.norm == "layernorm" else None,
+                            dbias=got["dbias"], workspace=got["ws"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    for a, b in zip(got["dres"] + got["dgat"], ref["dres"] + ref["dgat"]):
+        assert np.array_equal(compare.bf16_bits(a), compare.bf16_bits(b))
+    for name in ("dgamma", "dbias") + (("dbeta",) if w.norm == "layernorm" else ()):
+        assert torch.equal(got[name], ref[name]), name
+    # and against the oracle (same checks as the stored-mask backward)
+    C.check_bwd_rows(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], got, np.arange(w.tokens))
+    C.check_param_grads(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], got)
+
+
+def test_mask_free_backward_70b_sampled():
+    w = wl.WORKLOADS["bwd70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    got = C.alloc_bwd(w, 1)
+    C.sp.sp_norm_bwd_philox(dy, fwd["z"], fwd["mean"], fwd["rstd"], inp["gamma"], None, s=w.s,
+                            p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                            dresidual=got["dres"], dgathered=got["dgat"], dgamma=got["dgamma"],
+                            dbeta=got["dbeta"], dbias=got["dbias"], workspace=got["ws"])
+    torch.cuda.synchronize()
+    C.check_bwd_rows(w, fwd, inp["gamma"], dy, None, got, C.sample_tokens(w, 48))
+    C.check_param_grads(w, fwd, inp["gamma"], dy, None, got)

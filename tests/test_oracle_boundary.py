@@ -258,3 +258,37 @@ def test_backward_matches_torch_autograd(norm):
     assert np.array_equal(bwd["dgathered"][0], want)
     np.testing.assert_allclose(bwd["dbias"], (z.grad.numpy() * mask * float(ob.dropout_scale(w.p)))
                                .sum(axis=(0, 1)), rtol=1e-10, atol=1e-10)
+
+
+# ------------------------------------------------------- unfused boundary --
+
+def test_unfused_equals_fused_when_the_reduced_sum_is_bf16_exact():
+    # partials with few significant bits and t = 2: the float32 sum is itself a
+    # bf16 number, so rounding it (the unfused path) changes nothing
+    w = wl.Workload("u", t=2, b=1, s=16, h=64, draw_seed=13)
+    inp = _inputs(w)
+    rng = np.random.default_rng(2)
+    inp["partials"] = [(rng.integers(-8, 8, size=(1, 16, 64)) / 64).astype(np.float32)
+                       for _ in range(2)]
+    fused = _fwd(w, inp)
+    un = ob.unfused_fwd(inp["partials"], inp["residual"], inp["bias"], inp["gamma"],
+                        inp["beta"], eps=w.eps, p=w.p, seed=w.seed)
+    for k in range(w.t):
+        for key in ("z", "mask", "out"):
+            assert np.array_equal(fused[key][k], un[key][k]), key
+    assert np.array_equal(fused["gathered"][0], un["gathered"][0])
+
+
+def test_unfused_differs_from_fused_only_by_rounding_the_sum():
+    w = wl.Workload("u2", t=4, b=1, s=32, h=128, p=0.0, draw_seed=14)
+    inp = _inputs(w)
+    fused = _fwd(w, inp)
+    un = ob.unfused_fwd(inp["partials"], inp["residual"], inp["bias"], inp["gamma"],
+                        inp["beta"], eps=w.eps, p=w.p, seed=w.seed)
+    for k in range(w.t):
+        y32 = coll.reduce_scatter_seq(inp["partials"])[0][k]
+        # the reduce-scatter output differs from its fp32 value by <= half a bf16 ulp
+        assert np.all(np.abs(un["y_shards"][k] - y32) <= np.abs(y32) * 2.0 ** -8 + 1e-30)
+        # ... and Z by at most that plus Z's own rounding (a few bf16 ulps of |Z|)
+        dz = np.abs(fused["z"][k].astype(np.float64) - un["z"][k])
+        assert np.all(dz <= 2.0 ** -7 * np.abs(fused["z"][k]) + 2.0 ** -8 * np.abs(y32) + 1e-30)
