@@ -253,6 +253,29 @@ sp_status_t sp_norm_bwd_noalloc(const void* const* dy, const void* const* z,
                                 float* dbeta, float* dbias, int32_t* dev_status, void* stream);
 
 /*
+ * sp_rs_norm_bwd -- the backward entered through g, fused: the reduce-scatter
+ * of the t ranks' partial gradients of the gathered input (the gradient of an
+ * all-gather along s is a reduce-scatter along s, L7 §3.B) runs in the
+ * prologue of the norm / dropout backward, so no reduced dY is written or
+ * read.  Rank k's dY on its tokens is the float32 sum over r (ascending) of
+ * dy_partials[r], used unrounded; the rest is sp_norm_bwd.
+ *
+ * dy_partials [t] (b, s, h) bf16  rank r's partial gradient of the gathered
+ *                column-linear input (input)
+ * other arguments as for sp_norm_bwd (same workspace size); h <= 8192
+ * (SP_ERR_UNSUPPORTED above).
+ */
+sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
+                           const uint8_t* const* mask, const float* const* mean,
+                           const float* const* rstd, const void* gamma,
+                           const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                           int32_t t, double p, const int32_t* cu_seqlens, int32_t n_seqs,
+                           sp_norm_t norm, void* const* dresidual, void* const* dgathered,
+                           int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream);
+
+/*
  * sp_norm_bwd_philox -- the mask-free backward: sp_norm_bwd with the dropout
  * keep decisions drawn again from Philox4x32-10 instead of read from the
  * stored 1-byte mask.  Because the forward's generator is counter-based and

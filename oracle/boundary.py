@@ -342,3 +342,20 @@ def norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
         out[name] = None if (name == "dbeta" and norm != LAYERNORM) else acc[name]
         out[name + "_rss"] = np.sqrt(sq[name])
     return out
+
+
+def rs_norm_bwd(dy_partials, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
+                norm=LAYERNORM, n_gather=1):
+    """Backward entering through ``g``: the gradient of the all-gather is a
+    reduce-scatter along s (L7 §3.B).  Each rank's column-parallel linear
+    leaves a partial gradient of the full gathered input, (b, s, h); rank k's
+    dY is the float32, rank-ascending sum of those partials on its tokens
+    (not rounded: the fused boundary hands it to the norm backward directly),
+    then the shard backward of ``norm_bwd`` runs on it."""
+    dy_shards, rs_bytes = _coll.reduce_scatter_seq(dy_partials)
+    b = np.asarray(dy_partials[0]).shape[0]
+    out = norm_bwd([y.reshape(b, -1, y.shape[-1]) for y in dy_shards], z, mask, mean, rstd,
+                   gamma, dz_skip, p=p, norm=norm, n_gather=n_gather)
+    out["dy_shards"] = dy_shards
+    out["rs_remote_bytes"] = rs_bytes
+    return out

@@ -65,6 +65,8 @@ def load():
     lib.sp_shard_norm_fwd.argtypes = [
         _PP, _PP, _vp, _vp, _vp, _i64, _i64, _i64, _i32, ctypes.c_float, ctypes.c_double,
         _u64, _u64, _vp, _i32, _i32, _PP, _PP, _PP, _PP, _PP, _vp, _vp]
+    lib.sp_rs_norm_bwd.restype = _i32
+    lib.sp_rs_norm_bwd.argtypes = list(lib.sp_norm_bwd.argtypes)
     lib.sp_norm_bwd_philox.restype = _i32
     lib.sp_norm_bwd_philox.argtypes = [
         _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _u64, _u64, _vp,
@@ -306,6 +308,48 @@ def sp_norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlen
         _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev))
     _check(code)
+
+
+def sp_rs_norm_bwd(dy_partials, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
+                   cu_seqlens=None, norm="layernorm", dresidual, dgathered, dgamma=None,
+                   dbeta=None, dbias=None, workspace, status=None):
+    """Backward entered through g: reduce-scatter of the t partial gradients of
+    the gathered input, fused into the norm / dropout backward."""
+    lib = load()
+    t = len(dy_partials)
+    b, s, h = dy_partials[0].shape
+    dev = dy_partials[0].device
+    bf = torch.bfloat16
+    sizes = shard_sizes(s, t)
+    ln = norm == "layernorm"
+    for r in range(t):
+        _need(dy_partials[r], (b, s, h), bf, dev, f"dy_partials[{r}]")
+    for k in range(t):
+        _need(z[k], (b, sizes[k], h), bf, dev, f"z[{k}]")
+        _need(mask[k], (b, sizes[k], h), torch.uint8, dev, f"mask[{k}]")
+        _need(rstd[k], (b, sizes[k]), torch.float32, dev, f"rstd[{k}]")
+        if ln:
+            _need(mean[k], (b, sizes[k]), torch.float32, dev, f"mean[{k}]")
+        if dz_skip is not None:
+            _need(dz_skip[k], (b, sizes[k], h), bf, dev, f"dz_skip[{k}]")
+        _need(dresidual[k], (b, sizes[k], h), bf, dev, f"dresidual[{k}]")
+    for j, g in enumerate(dgathered):
+        _need(g, (b, s, h), bf, dev, f"dgathered[{j}]")
+    _need(gamma, (h,), bf, dev, "gamma")
+    for name, v in (("dgamma", dgamma), ("dbeta", dbeta), ("dbias", dbias)):
+        if v is not None:
+            _need(v, (h,), torch.float32, dev, name)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
+    st = device_status(dev) if status is None else status
+    _check(lib.sp_rs_norm_bwd(
+        _ptr_array(dy_partials), _ptr_array(z), _ptr_array(mask),
+        _ptr_array(mean) if ln else None, _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip),
+        b, s, h, t, float(p), cu, n_seqs, NORMS[norm], _ptr_array(dresidual),
+        _ptr_array(dgathered), len(dgathered), _ptr(dgamma), _ptr(dbeta) if ln else None,
+        _ptr(dbias), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(st),
+        _stream(dev)))
 
 
 def sp_norm_bwd_philox(dy, z, mean, rstd, gamma, dz_skip=None, *, s, p, seed, offset=0,

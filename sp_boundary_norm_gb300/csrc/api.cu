@@ -219,6 +219,34 @@ LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
 
 // Backward: a ring of whole rows (dY, Z, mask unless regenerated, optional
 // skip gradient).
+// Backward entered through g: t partial-gradient pieces per chunk stage, two
+// row buffers (Z, mask, skip), the reduced dY in float32.  The row buffers are
+// double-buffered, which is safe while the prefetch reaches at most one row
+// ahead: stages - 1 <= chunks per row.
+LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
+  const int64_t nvec = h / 8;
+  int threads, maxc;
+  if (nvec <= 64) {
+    threads = 64;
+    maxc = 1;
+  } else if (nvec <= 256) {
+    threads = 256;
+    maxc = 1;
+  } else {
+    threads = 512;
+    maxc = static_cast<int>((nvec + 511) / 512);
+  }
+  const size_t v16 = static_cast<size_t>(threads) * 16;
+  const size_t stage = static_cast<size_t>(t) * v16;
+  const size_t rb_item = v16 + threads * 8 + (has_skip ? v16 : 0);
+  const size_t fixed = 2 * maxc * rb_item + static_cast<size_t>(maxc) * 2 * v16 +
+                       2 * 32 * sizeof(float2);
+  static const int kOpts[] = {3, 2, 1};
+  const int want = maxc + 1 < 3 ? maxc + 1 : 3;
+  return pick_shape(1, threads, maxc, rows, stage, fixed, kOpts, 3, want, 1,
+                    [&](int st) { return rs_bwd_kernel(threads, maxc, t, st); });
+}
+
 LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
   const int64_t nvec = h / 8;
   int threads, maxc;
@@ -529,6 +557,12 @@ size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, s
     const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v & 2) != 0);
     if (ls.grid > grid) grid = ls.grid;
   }
+  if (h <= 8192) {
+    for (int v = 0; v < 2; ++v) {
+      const LaunchShape ls = rs_bwd_shape(b * s, h, t, v != 0);
+      if (ls.grid > grid) grid = ls.grid;
+    }
+  }
   return static_cast<size_t>(grid) * 3 * static_cast<size_t>(h) * sizeof(float);
 }
 
@@ -648,6 +682,118 @@ static sp_status_t norm_bwd_common(
     R.out[2] = dbias;
     e = launch_param_reduce(R, cs);
     if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd parameter reduce launch");
+  }
+  return SP_OK;
+}
+
+sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
+                           const uint8_t* const* mask, const float* const* mean,
+                           const float* const* rstd, const void* gamma,
+                           const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                           int32_t t, double p, const int32_t* cu_seqlens, int32_t n_seqs,
+                           sp_norm_t norm, void* const* dresidual, void* const* dgathered,
+                           int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
+  if (h > 8192)
+    return fail(SP_ERR_UNSUPPORTED, "sp_rs_norm_bwd: h = %lld above 8192", (long long)h);
+  if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
+    return fail(SP_ERR_INVALID_ARG, "unknown norm %d", (int)norm);
+  if (!(p >= 0.0 && p < 1.0)) return fail(SP_ERR_INVALID_ARG, "p = %g outside [0, 1)", p);
+  if (n_gather < 0 || n_gather > SP_MAX_RANKS)
+    return fail(SP_ERR_INVALID_ARG, "n_gather = %d outside [0, %d]", n_gather, SP_MAX_RANKS);
+  const bool ln = norm == SP_NORM_LAYERNORM;
+  const int64_t rows = b * s;
+  if (dgamma != nullptr && !aligned16(dgamma)) return fail(SP_ERR_MISALIGNED, "dgamma misaligned");
+  if (dbeta != nullptr && !aligned16(dbeta)) return fail(SP_ERR_MISALIGNED, "dbeta misaligned");
+  if (dbias != nullptr && !aligned16(dbias)) return fail(SP_ERR_MISALIGNED, "dbias misaligned");
+  if (rows == 0) {
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (dgamma) e = cudaMemsetAsync(dgamma, 0, h * 4, cs);
+    if (e == cudaSuccess && dbeta && ln) e = cudaMemsetAsync(dbeta, 0, h * 4, cs);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, h * 4, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_bwd zero fill");
+    return SP_OK;
+  }
+  const ShardMap map = make_map(b, s, h, t);
+  if ((st = check_ptrs(dy_partials, t, "dy_partials", true)) != SP_OK) return st;
+  if ((st = check_ptrs(z, t, "z", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(mask, t, "mask", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(rstd, t, "rstd", false, &map)) != SP_OK) return st;
+  if (ln && (st = check_ptrs(mean, t, "mean", false, &map)) != SP_OK) return st;
+  if (dz_skip != nullptr && (st = check_ptrs(dz_skip, t, "dz_skip", true, &map)) != SP_OK)
+    return st;
+  if ((st = check_ptrs(dresidual, t, "dresidual", true, &map)) != SP_OK) return st;
+  if ((st = check_ptrs(dgathered, n_gather, "dgathered", true)) != SP_OK) return st;
+  if ((st = check_vec(gamma, "gamma")) != SP_OK) return st;
+  if (dev_status != nullptr && (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
+  const bool has_skip = dz_skip != nullptr;
+  const LaunchShape ls = rs_bwd_shape(rows, h, t, has_skip);
+  const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(SP_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(SP_ERR_MISALIGNED, "workspace misaligned");
+  const size_t full = static_cast<size_t>(rows * h) * 2;
+  Ranges rg;
+  for (int r = 0; r < t; ++r) rg.add(dy_partials[r], full, false, "dy_partials", r);
+  for (int k = 0; k < t; ++k) {
+    const size_t n = static_cast<size_t>(shard_rows(map, k));
+    rg.add(z[k], n * h * 2, false, "z", k);
+    rg.add(mask[k], n * h, false, "mask", k);
+    rg.add(rstd[k], n * 4, false, "rstd", k);
+    if (ln) rg.add(mean[k], n * 4, false, "mean", k);
+    if (has_skip) rg.add(dz_skip[k], n * h * 2, false, "dz_skip", k);
+    rg.add(dresidual[k], n * h * 2, true, "dresidual", k);
+  }
+  for (int j = 0; j < n_gather; ++j) rg.add(dgathered[j], full, true, "dgathered", j);
+  rg.add(gamma, h * 2, false, "gamma", 0);
+  rg.add(dgamma, h * 4, true, "dgamma", 0);
+  if (ln) rg.add(dbeta, h * 4, true, "dbeta", 0);
+  rg.add(dbias, h * 4, true, "dbias", 0);
+  rg.add(workspace, need, true, "workspace", 0);
+  if ((st = rg.check()) != SP_OK) return st;
+
+  BwdParams P{};
+  P.map = map;
+  for (int r = 0; r < t; ++r) P.dy[r] = static_cast<const uint16_t*>(dy_partials[r]);
+  for (int k = 0; k < t; ++k) {
+    P.z[k] = static_cast<const uint16_t*>(z[k]);
+    P.mask[k] = mask[k];
+    P.rstd[k] = rstd[k];
+    P.mean[k] = ln ? mean[k] : nullptr;
+    P.dz_skip[k] = has_skip ? static_cast<const uint16_t*>(dz_skip[k]) : nullptr;
+    P.dresidual[k] = static_cast<uint16_t*>(dresidual[k]);
+  }
+  for (int j = 0; j < n_gather; ++j) P.dgathered[j] = static_cast<uint16_t*>(dgathered[j]);
+  P.gamma = static_cast<const uint16_t*>(gamma);
+  P.cu_seqlens = cu_seqlens;
+  P.n_seqs = n_seqs;
+  P.n_gather = n_gather;
+  P.norm = norm;
+  P.has_skip = has_skip ? 1 : 0;
+  P.scale = static_cast<float>(1.0 / (1.0 - p));
+  P.rows = rows;
+  P.ws = static_cast<float*>(workspace);
+  P.status = dev_status;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(rs_bwd_kernel(ls.threads, ls.maxc, t, ls.stages), ls, &P, cs);
+  if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_bwd launch");
+  if (dgamma || (dbeta && ln) || dbias) {
+    ParamReduceParams R{};
+    R.ws = P.ws;
+    R.nblk = ls.grid;
+    R.h = h;
+    R.out[0] = dgamma;
+    R.out[1] = ln ? dbeta : nullptr;
+    R.out[2] = dbias;
+    e = launch_param_reduce(R, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_bwd parameter reduce launch");
   }
   return SP_OK;
 }

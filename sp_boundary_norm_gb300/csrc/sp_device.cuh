@@ -185,6 +185,18 @@ __device__ __forceinline__ void mul2_to(float a0, float a1, float b, float& d0, 
       : "f"(a0), "f"(a1), "f"(b));
 }
 
+// (d0, d1) = (a0 * b0, a1 * b1)
+__device__ __forceinline__ void mul2_pair(float a0, float a1, float b0, float b1, float& d0,
+                                          float& d1) {
+  asm("{.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\t"
+      "mov.b64 {%0, %1}, d;}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
   asm("{.reg .b64 a, d;\n\t"
       "mov.b64 a, {%2, %3};\n\t"

@@ -105,6 +105,9 @@ const void* fwd_kernel(int threads, int t, int stages);
 const void* fwd_shard_kernel(int threads, int stages);
 const void* bwd_kernel(int threads, int maxc, int ring);
 const void* bwd_regen_kernel(int threads, int maxc, int ring);
+// Backward entered through g (reduce-scatter of t partial gradients fused):
+// (threads, chunks per row, ranks t, chunk stages).
+const void* rs_bwd_kernel(int threads, int maxc, int t, int stages);
 
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st);
 cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st);

@@ -457,3 +457,127 @@ def test_mask_free_backward_70b_sampled():
     torch.cuda.synchronize()
     C.check_bwd_rows(w, fwd, inp["gamma"], dy, None, got, C.sample_tokens(w, 48))
     C.check_param_grads(w, fwd, inp["gamma"], dy, None, got)
+
+
+# ------------------------------------------ backward entered through g
+
+def _rs_bwd_check(w, fwd, inp, parts, skip, out, tokens=None):
+    """dResidual / dYpre rows and parameter sums against the oracle, with dY
+    the float32 rank-ascending sum of the partial gradients on each shard."""
+    from oracle import collectives as coll
+    h = w.h
+    flat = [C.f32(x) for x in parts]
+    dy_shards, _ = coll.reduce_scatter_seq(flat)
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    g = C.f32(inp["gamma"])
+    acc = {n: np.zeros(h) for n in ("dgamma", "dbeta", "dbias")}
+    sq = {n: np.zeros(h) for n in acc}
+    scale = float(ob.dropout_scale(w.p))
+    for k in range(w.t):
+        n = w.b * (offs[k + 1] - offs[k])
+        if n == 0:
+            continue
+        rows = lambda x: x[k].reshape(-1, h)
+        one = ob.backward_rows(dy_shards[k].reshape(-1, h), C.f32(rows(fwd["z"])),
+                               rows(fwd["mask"]).cpu().numpy(),
+                               None if w.norm != "layernorm" else fwd["mean"][k].reshape(-1).cpu().numpy(),
+                               fwd["rstd"][k].reshape(-1).cpu().numpy(), g,
+                               None if skip is None else C.f32(rows(skip)), p=w.p, norm=w.norm)
+        sel = np.arange(n) if tokens is None else tokens[(tokens >= 0) & (tokens < n)]
+        dres = compare.bf16_bits(out["dres"][k].reshape(-1, h))
+        bad = compare.bf16_mismatch(dres[sel], one["dz"][sel], one["dz_magnitude"][sel])
+        assert not bad.any(), f"dresidual[{k}]: {bad.sum()} off"
+        for j, dg in enumerate(out["dgat"]):
+            blk = compare.bf16_bits(dg[:, offs[k]:offs[k + 1], :].reshape(-1, h))
+            bad = compare.bf16_mismatch(blk[sel], one["dypre_exact"][sel],
+                                        one["dz_magnitude"][sel] * scale)
+            assert not bad.any(), f"dgathered[{j}] shard {k}: {bad.sum()} off"
+        for name in acc:
+            terms = one[name + "_terms"]
+            if terms is not None:
+                acc[name] += terms.sum(axis=0)
+                sq[name] += (terms * terms).sum(axis=0)
+    for name in ("dgamma", "dbias") + (("dbeta",) if w.norm == "layernorm" else ()):
+        bad = compare.colsum_mismatch(out[name].cpu().numpy(), acc[name], np.sqrt(sq[name]))
+        assert not bad.any(), name
+
+
+def _run_rs_bwd(w, fwd, inp, parts, skip, n_gather=1):
+    out = C.alloc_bwd(w, n_gather)
+    C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                        skip, p=w.p, norm=w.norm, dresidual=out["dres"], dgathered=out["dgat"],
+                        dgamma=out["dgamma"],
+                        dbeta=out["dbeta"] if w.norm == "layernorm" else None,
+                        dbias=out["dbias"], workspace=out["ws"])
+    return out
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(t=3, s=48),
+                                     dict(b=2, s=40, t=4), dict(t=1), dict(h=5120, s=24),
+                                     dict(h=8, s=16), dict(h=2056, s=16), dict(p=0.0),
+                                     dict(t=16, s=32), dict(n_gather=0), dict(n_gather=3)])
+@pytest.mark.parametrize("with_skip", [False, True])
+def test_rs_norm_bwd_full_compare(variant, with_skip):
+    w = wl.Workload("rsb", t=2, b=1, s=64, h=512, draw_seed=81).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(99, C.DEV)
+    parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=C.DEV) * 0.5).to(torch.bfloat16)
+             for _ in range(w.t)]
+    skip = wl.backward_inputs(w, C.DEV, with_skip=True)["dz_skip"] if with_skip else None
+    out = _run_rs_bwd(w, fwd, inp, parts, skip, n_gather=w.n_gather)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    _rs_bwd_check(w, fwd, inp, parts, skip, out)
+
+
+def test_rs_norm_bwd_ragged_packed():
+    lengths = (5, 17, 3, 40, 1, 9)
+    w = wl.Workload("rsr", t=4, b=1, s=sum(lengths), h=256, seqlens=lengths, draw_seed=82)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(98, C.DEV)
+    parts = [torch.randn((1, w.s, w.h), generator=gen, device=C.DEV).to(torch.bfloat16)
+             for _ in range(w.t)]
+    out = C.alloc_bwd(w, 1)
+    cu = torch.from_numpy(wl.cu_seqlens(lengths)).to(C.DEV)
+    C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                        None, p=w.p, norm=w.norm, cu_seqlens=cu, dresidual=out["dres"],
+                        dgathered=out["dgat"], dgamma=out["dgamma"], dbeta=out["dbeta"],
+                        dbias=out["dbias"], workspace=out["ws"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    _rs_bwd_check(w, fwd, inp, parts, None, out)
+
+
+def test_rs_norm_bwd_70b_sampled():
+    w = wl.WORKLOADS["bwd70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(97, C.DEV)
+    parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=C.DEV) * 0.35).to(torch.bfloat16)
+             for _ in range(w.t)]
+    out = _run_rs_bwd(w, fwd, inp, parts, None)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    rng = np.random.default_rng(0)
+    tokens = np.unique(np.concatenate([[0, 1, 2047], rng.integers(0, 2048, 40)]))
+    _rs_bwd_check(w, fwd, inp, parts, None, out, tokens=tokens)
+
+
+def test_rs_norm_bwd_equals_unfused_reduce_then_norm_bwd_within_rounding():
+    """The unfused path rounds the reduced dY to bf16 before the norm backward;
+    with bf16-exact sums (few significant bits) the two agree bit for bit."""
+    w = wl.Workload("rse", t=4, b=1, s=64, h=1024, draw_seed=83)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(96, C.DEV)
+    parts = [(torch.randint(-8, 8, (1, w.s, w.h), generator=gen, device=C.DEV) / 64)
+             .to(torch.bfloat16) for _ in range(w.t)]
+    fused = _run_rs_bwd(w, fwd, inp, parts, None)
+    dy = [torch.empty((1, n, w.h), dtype=torch.bfloat16, device=C.DEV) for n in w.shard_sizes()]
+    C.sp.sp_reduce_scatter_seq(parts, dy)
+    plain = C.run_bwd(w, fwd, inp["gamma"], dy, None, n_gather=1)
+    torch.cuda.synchronize()
+    for a, b in zip(fused["dres"] + fused["dgat"], plain["dres"] + plain["dgat"]):
+        assert np.array_equal(compare.bf16_bits(a), compare.bf16_bits(b))

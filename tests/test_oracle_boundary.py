@@ -292,3 +292,58 @@ def test_unfused_differs_from_fused_only_by_rounding_the_sum():
         # ... and Z by at most that plus Z's own rounding (a few bf16 ulps of |Z|)
         dz = np.abs(fused["z"][k].astype(np.float64) - un["z"][k])
         assert np.all(dz <= 2.0 ** -7 * np.abs(fused["z"][k]) + 2.0 ** -8 * np.abs(y32) + 1e-30)
+
+
+# ------------------------------------------- backward entering through g
+
+def test_rs_norm_bwd_is_the_adjoint_of_gather_then_norm():
+    """Finite differences: L = sum_r <W_r, gathered O> with each rank's
+    column-linear partial gradient W_r; dL/dZ must equal the backward that
+    first reduce-scatters the W_r (L7 §3.B: bwd of g is a reduce-scatter)."""
+    w = wl.Workload("rb", t=3, b=1, s=9, h=16, p=0.3, draw_seed=15)
+    inp = _inputs(w)
+    rng = np.random.default_rng(4)
+    W = [rng.standard_normal((1, w.s, w.h)) for _ in range(w.t)]
+
+    def loss(res_):
+        r = _fwd(w, res_, exact=True, n_gather=0)
+        full = np.concatenate(r["out_exact"], axis=1)
+        return float(sum((Wr * full).sum() for Wr in W))
+
+    fwd = _fwd(w, inp, exact=True, n_gather=0)
+    bwd = ob.rs_norm_bwd(W, fwd["z"], fwd["mask"], fwd["mean64"], fwd["rstd64"], inp["gamma"],
+                         None, p=w.p, norm=w.norm, n_gather=1)
+    offs = coll.shard_offsets(w.s, w.t)
+    for k in range(w.t):
+        for i in range(offs[k + 1] - offs[k]):
+            for c in (0, 5, 15):
+                cp = {kk: ([a.astype(np.float64) for a in v] if isinstance(v, list) else
+                           (None if v is None else v.astype(np.float64))) for kk, v in inp.items()}
+                cm = {kk: ([a.copy() for a in v] if isinstance(v, list) else
+                           (None if v is None else v.copy())) for kk, v in cp.items()}
+                cp["residual"][k][0, i, c] += 1e-6
+                cm["residual"][k][0, i, c] -= 1e-6
+                fd = (loss(cp) - loss(cm)) / 2e-6
+                one = ob.backward_rows(bwd["dy_shards"][k][0], fwd["z"][k][0], fwd["mask"][k][0],
+                                       fwd["mean64"][k][0], fwd["rstd64"][k][0], inp["gamma"],
+                                       None, p=w.p, norm=w.norm)
+                assert one["dz"][i, c] == pytest.approx(fd, rel=1e-6, abs=1e-7)
+
+
+def test_rs_norm_bwd_equals_norm_bwd_on_the_reduced_gradient():
+    w = wl.Workload("rb2", t=4, b=2, s=12, h=32, draw_seed=16)
+    inp = _inputs(w)
+    fwd = _fwd(w, inp, n_gather=0)
+    rng = np.random.default_rng(5)
+    W = [(np.round(rng.standard_normal((2, 12, 32)) * 64) / 64).astype(np.float32)
+         for _ in range(w.t)]
+    a = ob.rs_norm_bwd(W, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                       p=w.p, n_gather=1)
+    shards, _ = coll.reduce_scatter_seq(W)
+    b = ob.norm_bwd(shards, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                    p=w.p, n_gather=1)
+    for k in range(w.t):
+        assert np.array_equal(a["dresidual"][k], b["dresidual"][k])
+    assert np.array_equal(a["dgamma"], b["dgamma"]) and np.array_equal(a["dbias"], b["dbias"])
+    # (t-1) ranks x b rows x s/t tokens x h x 2 bytes
+    assert a["rs_remote_bytes"] == [(w.t - 1) * 2 * (12 // 4) * 32 * 2] * w.t
