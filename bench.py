@@ -55,6 +55,15 @@ def unfused_fwd_bytes_per_token(t, h, n_gather, norm="layernorm"):
         + (2 * h + 2 * h * n_gather)
 
 
+def bwd_g_bytes_per_token(t, h, n_gather, norm="layernorm", fused=True):
+    """Backward entered through g: the t partial gradients of the gathered
+    input are read (fused: summed in the kernel; unfused: a reduce-scatter
+    writes the bf16 dY shard, which the norm backward reads again)."""
+    shard = bwd_bytes_per_token(h, n_gather, norm) - 2 * h   # without reading dY
+    rs = 2 * t * h if fused else 2 * t * h + 2 * h + 2 * h
+    return rs + shard
+
+
 def bwd_bytes_per_token(h, n_gather, norm="layernorm", skip=False):
     """Algorithmic bytes: dY, Z, mask, stats (+skip) read; dResidual, dYpre copies written."""
     stats = 8 if norm == "layernorm" else 4
@@ -215,9 +224,10 @@ class Step:
     the shards, all-gather as three calls (the ablation of the fusion).
     """
 
-    def __init__(self, w, device, n_gather=1, pipeline="fused", mask="stored"):
+    def __init__(self, w, device, n_gather=1, pipeline="fused", mask="stored", bwd_entry="shard"):
         self.pipeline = pipeline
         self.mask_mode = mask
+        self.bwd_entry = bwd_entry
         from sp_boundary_norm_gb300 import binding as sp
         self.sp, self.w, self.dev = sp, w, device
         self.inp = wl.forward_inputs(w, device)
@@ -237,6 +247,11 @@ class Step:
         if pipeline == "unfused":
             self.y = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
             self.o = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+        if bwd_entry == "g":
+            # each rank's partial gradient of the gathered (b, s, h) input
+            gen = wl.make_generator(w.draw_seed + 2000, device)
+            self.dy_parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=device)
+                              * 0.35).to(torch.bfloat16) for _ in range(w.t)]
 
     def fwd(self):
         w, i = self.w, self.inp
@@ -257,6 +272,16 @@ class Step:
 
     def bwd(self):
         w = self.w
+        if self.bwd_entry == "g":
+            if self.pipeline == "unfused":
+                self.sp.sp_reduce_scatter_seq(self.dy_parts, self.dy, cu_seqlens=self.cu)
+            else:
+                self.sp.sp_rs_norm_bwd(
+                    self.dy_parts, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"],
+                    None, p=w.p, norm=w.norm, cu_seqlens=self.cu, dresidual=self.dres,
+                    dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
+                    dbias=self.dbias, workspace=self.ws)
+                return
         if self.mask_mode == "regen":
             self.sp.sp_norm_bwd_philox(
                 self.dy, self.z, self.mean, self.rstd, self.inp["gamma"], None, s=w.s, p=w.p,
@@ -376,7 +401,8 @@ def run_ours(args):
     if args.norm is not None:
         w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
                     name=f"{w.name}-{args.norm}")
-    step = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask)
+    step = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
+                bwd_entry=args.bwd_entry)
     total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world, device)
     rejected = False
     if clocks_rejected(clocks):
@@ -389,8 +415,11 @@ def run_ours(args):
     fused = args.pipeline == "fused"
     fb = (fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
           unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm)) * w.tokens
-    bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm)
-          - (w.h if args.mask == "regen" else 0)) * w.tokens
+    if args.bwd_entry == "g":
+        bb = bwd_g_bytes_per_token(w.t, w.h, args.n_gather, w.norm, fused) * w.tokens
+    else:
+        bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm)
+              - (w.h if args.mask == "regen" else 0)) * w.tokens
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     peak, peak_kind = measured_peak()
@@ -413,7 +442,7 @@ def run_ours(args):
                                f"b={w.b}, s={w.s}, h={w.h}, p={w.p}, n_gather={args.n_gather}",
                    "t": w.t, "b": w.b, "s": w.s, "h": w.h, "norm": w.norm, "p": w.p,
                    "n_gather": args.n_gather, "pipeline": args.pipeline,
-                   "backward_mask": args.mask,
+                   "backward_mask": args.mask, "backward_entry": args.bwd_entry,
                    "l2": "inputs larger than L2 (2.1 GB of partials per step), no flush",
                    "parallelism": f"replicas x{world} (independent batches)"},
         "hbm_gbs": round((fb + bb) / (step_ms / 1e3) / 1e9, 1),
@@ -431,7 +460,8 @@ def run_ours(args):
                      "algorithmic_bytes": fb},
         "e2e": {"value": round(w.tokens * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": (3 if fused else 4 + (1 if args.n_gather else 0)) * args.steps,
+        "gpu_launches": ((3 if fused else 4 + (1 if args.n_gather else 0))
+                         + (1 if (args.bwd_entry == "g" and not fused) else 0)) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -512,6 +542,9 @@ def parse_args(argv=None):
     ap.add_argument("--norm", choices=["layernorm", "rmsnorm"], default=None,
                     help="override the norm")
     ap.add_argument("--n-gather", type=int, default=1)
+    ap.add_argument("--bwd-entry", choices=["shard", "g"], default="shard",
+                    help="g: the backward starts from each rank's partial gradient of the "
+                         "gathered input (reduce-scatter fused, or separate if unfused)")
     ap.add_argument("--mask", choices=["stored", "regen"], default="stored",
                     help="regen: the backward draws the dropout mask again (mask-free)")
     ap.add_argument("--pipeline", choices=["fused", "unfused"], default="fused",

@@ -81,3 +81,13 @@ def test_clock_rejection_rules():
     assert not bench.clocks_rejected({"reasons": ["sw_power_cap"], "sm_mhz": 1500,
                                       "sm_max_mhz": 2070})
     assert not bench.clocks_rejected({"reasons": [], "sm_mhz": 2070, "sm_max_mhz": 2070})
+
+
+def test_backward_through_g_byte_counts():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    h, t = 8192, 8
+    assert bench.bwd_g_bytes_per_token(t, h, 1, fused=True) == 23 * h + 8
+    assert bench.bwd_g_bytes_per_token(t, h, 1, fused=False) == 27 * h + 8
+    assert bench.unfused_fwd_bytes_per_token(t, h, 1) == 33 * h + 8
