@@ -190,30 +190,61 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
   return ls;
 }
 
-const int kFwdStages[] = {4, 3, 2};
-const int kBwdRing[] = {4, 3, 2};
+const int kFwdStages[] = {3, 2};
+const int kBwdRing[] = {3, 2};
+
+// Forward threads per block: the largest of 256, 160, 128, 64 that splits the
+// row's h/8 vectors into at least 4 (else at least 2) full chunks, so no
+// thread idles in a last partial chunk and the per-row work is spread over
+// several chunks; blocks per SM are then 512 / threads (16 warps).
+int fwd_threads(int64_t h) {
+  const int64_t nvec = h / 8;
+  static const int opts[] = {256, 160, 128, 64};
+  for (int min_chunks : {4, 2})
+    for (int n : opts)
+      if (nvec % n == 0 && nvec / n >= min_chunks) return n;
+  return nvec <= 64 ? 64 : 256;
+}
+
+// Backward (threads, chunks per row): two full chunks per thread where a
+// shape fits exactly (the per-thread parameter-gradient registers grow with
+// the chunks), else one, else the smallest shape that covers the row.
+void bwd_threads(int64_t h, int* threads, int* maxc) {
+  const int64_t nvec = h / 8;
+  static const int opts[][2] = {{512, 2}, {256, 2}, {128, 2}, {640, 1},
+                                {512, 1}, {256, 1}, {64, 1}};
+  for (const auto& o : opts) {
+    if (nvec == static_cast<int64_t>(o[0]) * o[1]) {
+      *threads = o[0];
+      *maxc = o[1];
+      return;
+    }
+  }
+  *threads = nvec <= 64 ? 64 : nvec <= 256 ? 256 : 512;
+  *maxc = nvec <= 512 ? 1 : nvec <= 1024 ? 2 : 4;
+}
 
 // Forward: every thread owns 8 channels of each chunk of 8 * threads channels;
 // one pipeline stage holds the chunk of the t partials and the residual, and
 // the row's Z waits in shared memory for the statistics.
 LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
-  const int threads = (h / 8 <= 64) ? 64 : 256;
+  const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
   const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float);
-  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 3,
-                    /*stages=*/3, /*blocks per SM=*/threads == 64 ? 4 : 2,
+  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 2,
+                    /*stages=*/3, /*blocks per SM=*/512 / threads,
                     [&](int st) { return fwd_kernel(threads, t, st); });
 }
 
 // The shard-input variant of the forward: two streams per stage.
 LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
-  const int threads = (h / 8 <= 64) ? 64 : 256;
+  const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(2) * threads * 16;
   const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float);
-  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 3,
-                    /*stages=*/4, /*blocks per SM=*/threads == 64 ? 4 : 2,
+  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 2,
+                    /*stages=*/3, /*blocks per SM=*/512 / threads,
                     [&](int st) { return fwd_shard_kernel(threads, st); });
 }
 
@@ -248,23 +279,13 @@ LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
 }
 
 LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
-  const int64_t nvec = h / 8;
   int threads, maxc;
-  if (nvec <= 64) {
-    threads = 64;
-    maxc = 1;
-  } else if (nvec <= 256) {
-    threads = 256;
-    maxc = 1;
-  } else {
-    threads = 512;
-    maxc = pow2_at_least(static_cast<int>((nvec + 511) / 512));
-  }
+  bwd_threads(h, &threads, &maxc);
   const size_t item =
       static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
   const size_t ring_row = item * maxc;
-  return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 3,
-                    /*ring=*/2, /*blocks per SM=*/threads == 512 ? 1 : 2, [&](int st) {
+  return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 2,
+                    /*ring=*/2, /*blocks per SM=*/threads <= 256 ? 512 / threads : 1, [&](int st) {
                       return regen ? bwd_regen_kernel(threads, maxc, st)
                                    : bwd_kernel(threads, maxc, st);
                     });

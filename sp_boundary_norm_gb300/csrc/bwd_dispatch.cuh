@@ -1,0 +1,34 @@
+// Launch-shape dispatch of the backward kernel template.
+#pragma once
+
+#include "bwd_kernel.cuh"
+
+namespace spb {
+
+template <int NTHR, int MAXC, bool REGEN>
+static const void* bwd_kernel_s(int ring) {
+  switch (ring) {
+    case 2: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 2, REGEN>);
+    case 3: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 3, REGEN>);
+    default: return nullptr;
+  }
+}
+
+// Instantiated shapes (threads, chunks per row): (64, 1), (128, 2), (256, 1),
+// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1); ring of 2 or 3 rows.
+template <bool REGEN>
+static const void* bwd_kernel_any(int threads, int maxc, int ring) {
+  switch (threads * 8 + maxc) {
+    case 64 * 8 + 1: return bwd_kernel_s<64, 1, REGEN>(ring);
+    case 128 * 8 + 2: return bwd_kernel_s<128, 2, REGEN>(ring);
+    case 256 * 8 + 1: return bwd_kernel_s<256, 1, REGEN>(ring);
+    case 256 * 8 + 2: return bwd_kernel_s<256, 2, REGEN>(ring);
+    case 512 * 8 + 1: return bwd_kernel_s<512, 1, REGEN>(ring);
+    case 512 * 8 + 2: return bwd_kernel_s<512, 2, REGEN>(ring);
+    case 512 * 8 + 4: return bwd_kernel_s<512, 4, REGEN>(ring);
+    case 640 * 8 + 1: return bwd_kernel_s<640, 1, REGEN>(ring);
+    default: return nullptr;
+  }
+}
+
+}  // namespace spb

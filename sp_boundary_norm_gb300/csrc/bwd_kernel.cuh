@@ -1,0 +1,224 @@
+// Norm / dropout backward kernel template (see bwd.cu for the design);
+// instantiated in bwd.cu (stored mask) and bwd_regen.cu (mask drawn again).
+#pragma once
+
+#include "sp_device.cuh"
+
+namespace spb {
+
+// REGEN = true: the mask-free variant; the dropout keep decisions are drawn
+// again from Philox4x32-10 at the element's global index (the forward's seed
+// and offset) instead of being read from the stored 1-byte mask.
+template <int NTHR, int MAXC, int RING, bool REGEN>
+__global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
+    norm_bwd_kernel(const BwdParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int h = static_cast<int>(P.map.h);   // <= SP_MAX_HIDDEN
+  constexpr int kChunk = 8 * NTHR;
+  const int nchunk = (h + kChunk - 1) / kChunk;
+  const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
+  const bool has_skip = P.has_skip != 0;
+  // one staged chunk ("item") of all threads: [dY | Z | mask | skip (optional)]
+  // (no mask slots in the mask-free variant)
+  constexpr int v16 = NTHR * 16;
+  constexpr int off_mask = 2 * v16;
+  constexpr int off_skip = off_mask + (REGEN ? 0 : NTHR * 8);
+  const int item_bytes = off_skip + (has_skip ? v16 : 0);
+  const int row_bytes = MAXC * item_bytes;
+  float2* red = reinterpret_cast<float2*>(smem + RING * row_bytes);   // [2][32]
+  const int c0 = tid * 8;
+  uint32_t valid = 0;   // bit ch: this thread has channels in chunk ch
+#pragma unroll
+  for (int ch = 0; ch < MAXC; ++ch)
+    if (ch < nchunk && ch * kChunk + c0 < h) valid |= 1u << ch;
+
+  if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
+
+  const int64_t G = gridDim.x;
+  const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
+
+  // gamma of this thread's channels, kept for every row
+  uint4 gam[MAXC];
+#pragma unroll
+  for (int ch = 0; ch < MAXC; ++ch)
+    gam[ch] = ((valid >> ch) & 1u) ? ldg16(P.gamma + ch * kChunk + c0) : make_uint4(0, 0, 0, 0);
+
+  // Stage the next row (all of its chunks, one cp.async group) into the next
+  // ring slot; rows are issued in order, so one cursor walks them.
+  RowCursor pf;
+  pf.init(P.map, blockIdx.x);
+  int64_t pf_ri = 0;
+  int pf_slot = 0;
+  auto issue_row = [&]() {
+    if (pf_ri < nrows) {
+      const int k = pf.k;
+      const int64_t lo0 = pf.local(P.map) * h + c0;
+      const uint16_t* dyp = P.dy[k] + lo0;
+      const uint16_t* zp = P.z[k] + lo0;
+      const uint8_t* mp = REGEN ? nullptr : P.mask[k] + lo0;
+      uint8_t* it0 = smem + pf_slot * row_bytes + tid * 16;
+#pragma unroll
+      for (int ch = 0; ch < MAXC; ++ch) {
+        if ((valid >> ch) & 1u) {
+          uint8_t* it = it0 + ch * item_bytes;
+          cp_async16(it, dyp + ch * kChunk);
+          cp_async16(it + v16, zp + ch * kChunk);
+          if (!REGEN) cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // 8 B apart
+          if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
+        }
+      }
+      if (++pf_ri < nrows) pf.advance(P.map, G);
+    }
+    cp_async_commit();
+    pf_slot = (pf_slot + 1 == RING) ? 0 : pf_slot + 1;
+  };
+
+#pragma unroll
+  for (int i = 0; i < RING - 1; ++i) issue_row();
+
+  float acc_g[MAXC][8], acc_b[MAXC][8], acc_bias[MAXC][8];
+#pragma unroll
+  for (int ch = 0; ch < MAXC; ++ch)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc_g[ch][e] = acc_b[ch][e] = acc_bias[ch][e] = 0.f;
+
+  // statistics of the current row, loaded one row ahead
+  RowCursor cur, nxt;
+  cur.init(P.map, blockIdx.x);
+  nxt = cur;
+  float cur_mean = 0.f, cur_rstd = 0.f;
+  if (nrows > 0) {
+    const int64_t l0 = cur.local(P.map);
+    cur_rstd = P.rstd[cur.k][l0];
+    if (is_ln) cur_mean = P.mean[cur.k][l0];
+  }
+
+  int slot_sel = 0;
+  int slot = 0;   // ring slot of the current row
+  const float fh = static_cast<float>(h);
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    if (ri > 0) cur = nxt;
+    const int64_t row = cur.row;
+    const int k = cur.k;
+    const int64_t local = cur.local(P.map);
+    float nx_mean = 0.f, nx_rstd = 0.f;
+    if (ri + 1 < nrows) {
+      nxt.advance(P.map, G);
+      const int64_t l1 = nxt.local(P.map);
+      nx_rstd = P.rstd[nxt.k][l1];
+      if (is_ln) nx_mean = P.mean[nxt.k][l1];
+    }
+    const float mean = cur_mean, rstd = cur_rstd;
+
+    issue_row();                    // row ri + RING - 1 refills the slot row ri - 1 used
+    cp_async_wait<RING - 1>();      // row ri has landed
+    const uint8_t* it0 = smem + slot * row_bytes + tid * 16;
+    slot = (slot + 1 == RING) ? 0 : slot + 1;
+
+    // ---- pass 1: the two row sums, and dgamma / dbeta terms --------------
+    // x_hat = (z - mean) * rstd (LN) or z * rstd (RMS); dxh = dY * gamma is an
+    // exact product of two bf16 values
+    const float nmean = is_ln ? -mean : 0.f;
+    float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < MAXC; ++ch) {
+      if ((valid >> ch) & 1u) {
+        const uint8_t* it = it0 + ch * item_bytes;
+        const uint4 dyv = lds16(it);
+        const uint4 zv = lds16(it + v16);
+        float xh[8], dxh[8], dy[8];
+        add8_bf16_bcast(zv, nmean, xh);             // z - mean
+        fma8_bf16_bcast(dyv, gam[ch], 0.f, dxh);    // dY * gamma
+        if (is_ln) add8_bf16(dyv, acc_b[ch]);       // dbeta terms
+        unpack8(dyv, dy);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          mul2(xh[e], xh[e + 1], rstd, rstd);
+          add2(s1a, s1b, dxh[e], dxh[e + 1]);
+          fma2(s2a, s2b, dxh[e], dxh[e + 1], xh[e], xh[e + 1]);
+          fma2(acc_g[ch][e], acc_g[ch][e + 1], dy[e], dy[e + 1], xh[e], xh[e + 1]);
+        }
+      }
+    }
+
+    const float2 s = block_sum2(s1a + s1b, s2a + s2b, red + 32 * slot_sel);
+    slot_sel ^= 1;
+    const float nm1 = is_ln ? -(s.x / fh) : 0.f;
+    const float nm2r = -(s.y / fh) * rstd;
+
+    // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
+    // dZ = rstd * (dxh - m1 - (z - mean) * rstd * m2)
+    uint16_t* dres_row = P.dresidual[k] + local * h + c0;
+    const int64_t grow = row * h + c0;
+    uint16_t* dg0_row = P.n_gather > 0 ? P.dgathered[0] + grow : nullptr;
+#pragma unroll
+    for (int ch = 0; ch < MAXC; ++ch) {
+      if ((valid >> ch) & 1u) {
+        const uint8_t* it = it0 + ch * item_bytes;
+        const uint4 dyv = lds16(it);
+        const uint4 zv = lds16(it + v16);
+        uint2 mk;
+        if (REGEN) {
+          const uint64_t q = static_cast<uint64_t>(grow + ch * kChunk) >> 2;
+          const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
+                                                   static_cast<uint32_t>(q >> 32), P.off0, P.off1),
+                                        P.key0, P.key1);
+          const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+                                                   static_cast<uint32_t>((q + 1) >> 32), P.off0,
+                                                   P.off1),
+                                        P.key0, P.key1);
+          mk = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
+        } else {
+          mk = lds8(it + off_mask - tid * 8);
+        }
+        float zc[8], dz[8], dp[8];
+        add8_bf16_bcast(zv, nmean, zc);           // z - mean
+        fma8_bf16_bcast(dyv, gam[ch], nm1, dz);  // dxh - m1
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          fma2(dz[e], dz[e + 1], zc[e], zc[e + 1], nm2r, nm2r);
+          mul2(dz[e], dz[e + 1], rstd, rstd);
+        }
+        if (has_skip) add8_bf16(lds16(it + off_skip), dz);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) mul2_to(dz[e], dz[e + 1], P.scale, dp[e], dp[e + 1]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          // mask bytes are 0 or 1: bit 0 of byte e decides
+          const bool kept = ((e < 4 ? mk.x : mk.y) & (1u << (8 * (e & 3)))) != 0u;
+          dp[e] = kept ? dp[e] : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) add2(acc_bias[ch][e], acc_bias[ch][e + 1], dp[e], dp[e + 1]);
+        st16_stream(dres_row + ch * kChunk, pack8(dz));
+        const uint4 pb = pack8(dp);
+        if (dg0_row != nullptr) st16_stream(dg0_row + ch * kChunk, pb);
+        for (int j = 1; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
+      }
+    }
+    cur_mean = nx_mean;
+    cur_rstd = nx_rstd;
+  }
+  cp_async_wait<0>();
+
+  // per-block partials: ws[block][0|1|2][c] = dgamma | dbeta | dbias terms
+  float* wsb = P.ws + static_cast<int64_t>(blockIdx.x) * 3 * h;
+#pragma unroll
+  for (int ch = 0; ch < MAXC; ++ch) {
+    const int c = ch * kChunk + c0;
+    if ((valid >> ch) & 1u) {
+      float4* dg = reinterpret_cast<float4*>(wsb + c);
+      float4* db = reinterpret_cast<float4*>(wsb + h + c);
+      float4* dc = reinterpret_cast<float4*>(wsb + 2 * h + c);
+      dg[0] = make_float4(acc_g[ch][0], acc_g[ch][1], acc_g[ch][2], acc_g[ch][3]);
+      dg[1] = make_float4(acc_g[ch][4], acc_g[ch][5], acc_g[ch][6], acc_g[ch][7]);
+      db[0] = make_float4(acc_b[ch][0], acc_b[ch][1], acc_b[ch][2], acc_b[ch][3]);
+      db[1] = make_float4(acc_b[ch][4], acc_b[ch][5], acc_b[ch][6], acc_b[ch][7]);
+      dc[0] = make_float4(acc_bias[ch][0], acc_bias[ch][1], acc_bias[ch][2], acc_bias[ch][3]);
+      dc[1] = make_float4(acc_bias[ch][4], acc_bias[ch][5], acc_bias[ch][6], acc_bias[ch][7]);
+    }
+  }
+}
+
+}  // namespace spb

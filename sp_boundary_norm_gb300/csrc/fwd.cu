@@ -8,7 +8,7 @@
 // of that token once, and writes Z, the mask, the statistics and the
 // normalised row straight into the all-gather destination(s).
 //
-// Work layout: a persistent grid (two blocks per SM); block b processes
+// Work layout: a persistent grid (16 warps per SM); block b processes
 // tokens b, b + G, b + 2G, ...  A row of h channels is cut into chunks of 8*T
 // channels (T = threads); in each chunk thread i owns channels [8i, 8i+8).
 // Every thread streams its own 16-byte pieces of the t + 1 input rows into
@@ -19,248 +19,30 @@
 // are the row reductions of the norm.  The chunk loop is not unrolled (the
 // Philox rounds make its body long): Z of the row waits for the statistics
 // in the thread's own shared-memory slots rather than in registers.
-#include "sp_device.cuh"
+#include "fwd_kernel.cuh"
 
 namespace spb {
 
-// SHARD = false: the fused boundary (inputs: the t full partials; output:
-// the gathered full buffers).  SHARD = true: the middle step of the unfused
-// boundary (input: each rank's already reduced shard, one stream; output: O
-// of each shard in its own buffer; P.partials / P.gathered hold per-shard
-// pointers).  Dropout draws use the token's index in the full sequence in
-// both cases.
-template <int NTHR, int STAGES, int TT, bool SHARD>
-__global__ void __launch_bounds__(NTHR, (NTHR >= 256 ? 2 : 4))
-    rs_norm_fwd_kernel(const FwdParams P) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int tid = threadIdx.x;
-  // input streams summed per element (compile-time when specialised)
-  const int t = SHARD ? 1 : (TT > 0 ? TT : P.map.t);
-  const int64_t h = P.map.h;
-  constexpr int kChunk = 8 * NTHR;
-  const int nchunk = static_cast<int>((h + kChunk - 1) / kChunk);
-  constexpr int kStream = NTHR * 16;
-  const int stage_bytes = (t + 1) * kStream;
-  uint8_t* zbuf = smem + STAGES * stage_bytes + tid * 16;   // own slots, stride kStream
-  float* red = reinterpret_cast<float*>(smem + STAGES * stage_bytes + nchunk * kStream);
-  const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
-
-  if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
-
-  const int64_t G = gridDim.x;
-  const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
-  const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
-
-  // ---- prefetch cursor: the next (row, chunk) item to stage -------------
-  // pf_goff: element offset of (row, chunk) in the (b, s, h) partials;
-  // pf_roff: element offset in the residual shard of that row.
-  RowCursor pf;
-  pf.init(P.map, blockIdx.x);
-  int64_t pf_ri = 0, pf_goff = pf.row * h + c0, pf_roff = pf.local(P.map) * h + c0;
-  int pf_chunk = 0, pf_stage = 0;
-
-  auto issue_next = [&]() {
-    if (pf_ri < nrows) {
-      if (pf_chunk * kChunk + c0 < h) {
-        uint8_t* slot = smem + pf_stage * stage_bytes + tid * 16;
-        if (SHARD) {
-          cp_async16(slot, P.partials[pf.k] + pf_roff);
-        } else {
-#pragma unroll
-          for (int r = 0; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
-            if (TT > 0 || r < t) cp_async16(slot + r * kStream, P.partials[r] + pf_goff);
-        }
-        cp_async16(slot + t * kStream, P.residual[pf.k] + pf_roff);
-      }
-      if (++pf_chunk == nchunk) {
-        pf_chunk = 0;
-        if (++pf_ri < nrows) {
-          pf.advance(P.map, G);
-          pf_goff = pf.row * h + c0;
-          pf_roff = pf.local(P.map) * h + c0;
-        }
-      } else {
-        pf_goff += kChunk;
-        pf_roff += kChunk;
-      }
-    }
-    cp_async_commit();
-    pf_stage = (pf_stage + 1 == STAGES) ? 0 : pf_stage + 1;
-  };
-
-#pragma unroll
-  for (int i = 0; i < STAGES - 1; ++i) issue_next();
-
-  RowCursor cur;
-  cur.init(P.map, blockIdx.x);
-  int stage = 0;
-  int slot_sel = 0;
-  const float fh = static_cast<float>(h);
-  for (int64_t ri = 0; ri < nrows; ++ri) {
-    if (ri > 0) cur.advance(P.map, G);
-    const int64_t row = cur.row;
-    const int k = cur.k;
-    const int64_t local = cur.local(P.map);
-    uint16_t* zrow = P.z[k] + local * h + c0;
-    uint8_t* mrow = P.mask[k] + local * h + c0;
-    const uint64_t e_row = static_cast<uint64_t>(row * h + c0);   // global element index
-
-    // ---- pass 1: g* sum, bias, dropout, residual -> Z (stored) ----------
-    float lsum = 0.f;
-#pragma unroll 1
-    for (int ch = 0; ch < nchunk; ++ch) {
-      issue_next();
-      cp_async_wait<STAGES - 1>();
-      const int cc = ch * kChunk;
-      if (cc + c0 < h) {
-        const uint8_t* slot = smem + stage * stage_bytes + tid * 16;
-        const uint4 bv = ldg16(P.bias + cc + c0);
-        // g*: float32 sum of the t partials, ranks in ascending order
-        // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
-        float y[8];
-        unpack8(lds16(slot), y);
-        if (!SHARD) {
-#pragma unroll
-          for (int r = 1; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
-            if (TT > 0 || r < t) add8_bf16(lds16(slot + r * kStream), y);
-        }
-        add8_bf16(bv, y);   // + bias
-        // dropout: element e keeps iff its Philox word >= thr
-        uint2 keep = make_uint2(0x01010101u, 0x01010101u);
-        if (P.thr) {
-          const uint64_t q = (e_row + cc) >> 2;
-          const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
-                                                   static_cast<uint32_t>(q >> 32), P.off0, P.off1),
-                                        P.key0, P.key1);
-          const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
-                                                   static_cast<uint32_t>((q + 1) >> 32), P.off0,
-                                                   P.off1),
-                                        P.key0, P.key1);
-          const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-          float ys[8];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) mul2_to(y[e], y[e + 1], P.scale, ys[e], ys[e + 1]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = (u[e] >= P.thr) ? ys[e] : 0.f;
-          keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
-        }
-        // (with p == 0 the scale is exactly 1 and y * 1 == y)
-        add8_bf16(lds16(slot + t * kStream), y);   // + residual -> Z in fp32
-        const uint4 zb = pack8(y);                 // Z = bf16_rne(...)
-        st16_stream(zrow + cc, zb);
-        st8_stream(mrow + cc, keep);
-        *reinterpret_cast<uint4*>(zbuf + ch * kStream) = zb;
-        // the norm sees the stored bf16 values
-        float l2[2] = {0.f, 0.f};
-        if (is_ln) {
-          add2_bf16(zb.x, l2[0], l2[1]);
-          add2_bf16(zb.y, l2[0], l2[1]);
-          add2_bf16(zb.z, l2[0], l2[1]);
-          add2_bf16(zb.w, l2[0], l2[1]);
-        } else {
-          fma2_bf16(zb.x, zb.x, l2[0], l2[1]);
-          fma2_bf16(zb.y, zb.y, l2[0], l2[1]);
-          fma2_bf16(zb.z, zb.z, l2[0], l2[1]);
-          fma2_bf16(zb.w, zb.w, l2[0], l2[1]);
-        }
-        lsum += l2[0] + l2[1];
-      }
-      stage = (stage + 1 == STAGES) ? 0 : stage + 1;
-    }
-
-    // ---- token-wise statistics over h ------------------------------------
-    float mean = 0.f, rstd;
-    if (is_ln) {
-      mean = block_sum(lsum, red + 32 * slot_sel) / fh;
-      slot_sel ^= 1;
-      float lsqa = 0.f, lsqb = 0.f;
-      const float nmean = -mean;
-#pragma unroll 1
-      for (int ch = 0; ch < nchunk; ++ch) {
-        if (ch * kChunk + c0 < h) {
-          float d[8];
-          add8_bf16_bcast(lds16(zbuf + ch * kStream), nmean, d);   // z - mean
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
-        }
-      }
-      const float var = block_sum(lsqa + lsqb, red + 32 * slot_sel) / fh;
-      slot_sel ^= 1;
-      rstd = rsqrtf(var + P.eps);
-    } else {
-      const float ms = block_sum(lsum, red + 32 * slot_sel) / fh;
-      slot_sel ^= 1;
-      rstd = rsqrtf(ms + P.eps);
-    }
-
-    // ---- normalise and write into the all-gather destination(s) ----------
-    const int64_t orow = row * h + c0;
-    uint16_t* g0_row = SHARD ? P.gathered[k] + local * h + c0
-                             : (P.n_gather > 0 ? P.gathered[0] + orow : nullptr);
-#pragma unroll 1
-    for (int ch = 0; ch < nchunk; ++ch) {
-      const int cc = ch * kChunk;
-      if (cc + c0 < h) {
-        const uint4 zv = lds16(zbuf + ch * kStream);
-        const uint4 gv = ldg16(P.gamma + cc + c0);
-        float o[8];
-        if (is_ln) {
-          float g[8], bt[8];
-          unpack8(gv, g);
-          unpack8(ldg16(P.beta + cc + c0), bt);
-          add8_bf16_bcast(zv, -mean, o);   // z - mean
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            mul2(o[e], o[e + 1], rstd, rstd);
-            fma2(bt[e], bt[e + 1], o[e], o[e + 1], g[e], g[e + 1]);   // * gamma + beta
-            o[e] = bt[e];
-            o[e + 1] = bt[e + 1];
-          }
-        } else {
-          fma8_bf16_bcast(zv, gv, 0.f, o);   // z * gamma, exact
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) mul2(o[e], o[e + 1], rstd, rstd);
-        }
-        const uint4 ob = pack8(o);
-        if (g0_row != nullptr) st16_stream(g0_row + cc, ob);
-        if (!SHARD)
-          for (int j = 1; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
-      }
-    }
-    if (tid == 0) {
-      if (is_ln) P.mean[k][local] = mean;
-      P.rstd[k][local] = rstd;
-    }
-  }
-  cp_async_wait<0>();
-}
-
-template <int NTHR, int TT, bool SHARD>
+template <int NTHR, int TT>
 static const void* fwd_kernel_s(int stages) {
   switch (stages) {
-    case 2: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 2, TT, SHARD>);
-    case 3: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 3, TT, SHARD>);
-    case 4: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 4, TT, SHARD>);
+    case 2: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 2, TT, false>);
+    case 3: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 3, TT, false>);
     default: return nullptr;
   }
 }
 
-// Instantiated shapes: 64 threads for h <= 512, else 256; pipeline depth 2, 3
-// or 4 chunks; t either a run-time value or the compile-time 8.
+// Instantiated shapes: 64, 128, 160 or 256 threads per block; pipeline depth
+// 2 or 3 chunks; t either a run-time value or the compile-time 8.
 const void* fwd_kernel(int threads, int t, int stages) {
   const bool t8 = (t == 8);
-  if (threads == 64)
-    return t8 ? fwd_kernel_s<64, 8, false>(stages) : fwd_kernel_s<64, 0, false>(stages);
-  if (threads == 256)
-    return t8 ? fwd_kernel_s<256, 8, false>(stages) : fwd_kernel_s<256, 0, false>(stages);
-  return nullptr;
-}
-
-// The shard-input / shard-output variant (one input stream).
-const void* fwd_shard_kernel(int threads, int stages) {
-  if (threads == 64) return fwd_kernel_s<64, 1, true>(stages);
-  if (threads == 256) return fwd_kernel_s<256, 1, true>(stages);
-  return nullptr;
+  switch (threads) {
+    case 64: return t8 ? fwd_kernel_s<64, 8>(stages) : fwd_kernel_s<64, 0>(stages);
+    case 128: return t8 ? fwd_kernel_s<128, 8>(stages) : fwd_kernel_s<128, 0>(stages);
+    case 160: return t8 ? fwd_kernel_s<160, 8>(stages) : fwd_kernel_s<160, 0>(stages);
+    case 256: return t8 ? fwd_kernel_s<256, 8>(stages) : fwd_kernel_s<256, 0>(stages);
+    default: return nullptr;
+  }
 }
 
 }  // namespace spb
