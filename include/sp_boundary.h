@@ -311,13 +311,18 @@ sp_status_t sp_debug_inject(sp_status_t code);
 /*
  * sp_debug_tune -- tuning hook: override the launch shape chosen for the
  * forward (kernel 0) or backward (kernel 1) row kernels: `stages` = cp.async
- * pipeline depth (0 = default), `blocks_per_sm` = resident blocks per SM the
- * grid is sized for (0 = default).  Values that do not fit shared memory are
- * reduced.  Affects sp_norm_bwd_workspace_bytes, so set it before sizing the
- * workspace.  Results do not depend on it except the float rounding of the
- * parameter-gradient sums (their block partition changes).
+ * pipeline depth, `blocks_per_sm` = resident blocks per SM the grid is sized
+ * for, `threads` = threads per block (forward: 64, 128, 160 or 256), `chunks`
+ * = chunks per row (backward, with `threads`: one of the instantiated pairs);
+ * 0 keeps the default rule for that field.  Values that do not fit shared
+ * memory are reduced; shapes that are not instantiated are ignored.  Affects
+ * sp_norm_bwd_workspace_bytes, so set it before sizing the workspace.  Results
+ * do not depend on it except the float rounding of sums whose partition
+ * changes (row statistics with the thread count, parameter gradients with the
+ * grid).
  */
-sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm);
+sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm,
+                          int32_t threads, int32_t chunks);
 
 /*
  * sp_debug_philox -- evaluate the library's device Philox4x32-10 on n

@@ -82,7 +82,7 @@ def load():
     lib.sp_debug_inject.restype = _i32
     lib.sp_debug_inject.argtypes = [_i32]
     lib.sp_debug_tune.restype = _i32
-    lib.sp_debug_tune.argtypes = [_i32, _i32, _i32]
+    lib.sp_debug_tune.argtypes = [_i32, _i32, _i32, _i32, _i32]
     lib.sp_debug_philox.restype = _i32
     lib.sp_debug_philox.argtypes = [_vp, _vp, _i64, _vp]
     _lib = lib
@@ -442,8 +442,9 @@ def sp_debug_inject(code):
     load().sp_debug_inject(int(code))
 
 
-def sp_debug_tune(kernel, stages=0, blocks_per_sm=0):
-    _check(load().sp_debug_tune(int(kernel), int(stages), int(blocks_per_sm)))
+def sp_debug_tune(kernel, stages=0, blocks_per_sm=0, threads=0, chunks=0):
+    _check(load().sp_debug_tune(int(kernel), int(stages), int(blocks_per_sm), int(threads),
+                                int(chunks)))
 
 
 def sp_debug_philox(ctr_key):

@@ -17,8 +17,9 @@ namespace {
 
 thread_local char g_err[512] = "";
 std::atomic<int> g_inject{SP_OK};
-// Launch-shape overrides for tuning sweeps: [kernel][stages, blocks per SM].
-std::atomic<int> g_tune[2][2] = {{{0}, {0}}, {{0}, {0}}};
+// Launch-shape overrides for tuning sweeps: [kernel][stages, blocks per SM,
+// threads, chunks per row (backward only)]; 0 = the default rule.
+std::atomic<int> g_tune[2][4] = {{{0}, {0}, {0}, {0}}, {{0}, {0}, {0}, {0}}};
 
 sp_status_t fail(sp_status_t code, const char* fmt, ...) {
   va_list ap;
@@ -137,6 +138,55 @@ constexpr size_t kSmemPerSm = 228 * 1024;     // sm_100-class shared memory per 
 constexpr size_t kSmemPerBlock = 227 * 1024;  // opt-in maximum per block
 constexpr size_t kReserve = 1024;             // per-block reservation
 
+// Launch shapes are pure functions of (kernel kind, rows, h, t, flags, device,
+// tuning overrides); caching them keeps the per-call host cost to the
+// argument checks, which matters for short kernels.
+struct ShapeKey {
+  int kind, t, flags, device, tune;
+  int64_t rows, h;
+  bool operator==(const ShapeKey& o) const {
+    return kind == o.kind && t == o.t && flags == o.flags && device == o.device &&
+           tune == o.tune && rows == o.rows && h == o.h;
+  }
+};
+
+struct ShapeCache {
+  std::mutex mu;
+  static constexpr int kSlots = 64;
+  ShapeKey key[kSlots];
+  LaunchShape val[kSlots];
+  int used = 0, next = 0;
+};
+
+ShapeCache g_shapes;
+std::atomic<int> g_tune_epoch{0};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  return dev;
+}
+
+template <typename Make>
+LaunchShape cached_shape(int kind, int64_t rows, int64_t h, int t, int flags, Make make) {
+  const ShapeKey k{kind, t, flags, current_device(), g_tune_epoch.load(), rows, h};
+  {
+    std::lock_guard<std::mutex> lock(g_shapes.mu);
+    for (int i = 0; i < g_shapes.used; ++i)
+      if (g_shapes.key[i] == k) return g_shapes.val[i];
+  }
+  const LaunchShape ls = make();
+  std::lock_guard<std::mutex> lock(g_shapes.mu);
+  const int slot = g_shapes.used < ShapeCache::kSlots ? g_shapes.used++ : g_shapes.next;
+  g_shapes.next = (slot + 1) % ShapeCache::kSlots;
+  g_shapes.key[slot] = k;
+  g_shapes.val[slot] = ls;
+  return ls;
+}
+
 // Choose the pipeline depth (`stages`: chunks for the forward, rows for the
 // backward) and blocks per SM: start from the requested pair and shrink, blocks
 // first, until the shared memory fits; then cap the grid at what the
@@ -199,6 +249,8 @@ const int kBwdRing[] = {3, 2};
 // several chunks; blocks per SM are then 512 / threads (16 warps).
 int fwd_threads(int64_t h) {
   const int64_t nvec = h / 8;
+  const int forced = g_tune[0][2].load();
+  if (forced != 0 && fwd_kernel(forced, 0, 2) != nullptr) return forced;
   static const int opts[] = {256, 160, 128, 64};
   for (int min_chunks : {4, 2})
     for (int n : opts)
@@ -211,6 +263,13 @@ int fwd_threads(int64_t h) {
 // the chunks), else one, else the smallest shape that covers the row.
 void bwd_threads(int64_t h, int* threads, int* maxc) {
   const int64_t nvec = h / 8;
+  const int ft = g_tune[1][2].load(), fc = g_tune[1][3].load();
+  if (ft != 0 && fc != 0 && static_cast<int64_t>(ft) * fc * 8 >= h &&
+      bwd_kernel(ft, fc, 2) != nullptr) {
+    *threads = ft;
+    *maxc = fc;
+    return;
+  }
   static const int opts[][2] = {{512, 2}, {256, 2}, {128, 2}, {640, 1},
                                 {512, 1}, {256, 1}, {64, 1}};
   for (const auto& o : opts) {
@@ -227,7 +286,7 @@ void bwd_threads(int64_t h, int* threads, int* maxc) {
 // Forward: every thread owns 8 channels of each chunk of 8 * threads channels;
 // one pipeline stage holds the chunk of the t partials and the residual, and
 // the row's Z waits in shared memory for the statistics.
-LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
+LaunchShape fwd_shape_uncached(int64_t rows, int64_t h, int t) {
   const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
@@ -238,7 +297,7 @@ LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
 }
 
 // The shard-input variant of the forward: two streams per stage.
-LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
+LaunchShape fwd_shard_shape_uncached(int64_t rows, int64_t h) {
   const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(2) * threads * 16;
@@ -254,7 +313,7 @@ LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
 // row buffers (Z, mask, skip), the reduced dY in float32.  The row buffers are
 // double-buffered, which is safe while the prefetch reaches at most one row
 // ahead: stages - 1 <= chunks per row.
-LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
+LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip) {
   const int64_t nvec = h / 8;
   int threads, maxc;
   if (nvec <= 64) {
@@ -278,7 +337,7 @@ LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
                     [&](int st) { return rs_bwd_kernel(threads, maxc, t, st); });
 }
 
-LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
+LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool regen) {
   int threads, maxc;
   bwd_threads(h, &threads, &maxc);
   const size_t item =
@@ -291,9 +350,59 @@ LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false
                     });
 }
 
+LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
+  return cached_shape(0, rows, h, t, 0, [&] { return fwd_shape_uncached(rows, h, t); });
+}
+
+LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
+  return cached_shape(1, rows, h, 1, 0, [&] { return fwd_shard_shape_uncached(rows, h); });
+}
+
+LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
+  return cached_shape(2, rows, h, t, has_skip ? 1 : 0,
+                      [&] { return rs_bwd_shape_uncached(rows, h, t, has_skip); });
+}
+
+LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
+  return cached_shape(3, rows, h, 0, (has_skip ? 1 : 0) | (regen ? 2 : 0),
+                      [&] { return bwd_shape_uncached(rows, h, has_skip, regen); });
+}
+
+// The dynamic shared-memory opt-in of each kernel, set once per (kernel,
+// device) to the largest size requested so far.
+struct AttrCache {
+  std::mutex mu;
+  static constexpr int kSlots = 256;
+  const void* fn[kSlots];
+  int device[kSlots];
+  size_t smem[kSlots];
+  int used = 0;
+};
+AttrCache g_attr;
+
+cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_attr.mu);
+  int i = 0;
+  for (; i < g_attr.used; ++i)
+    if (g_attr.fn[i] == fn && g_attr.device[i] == dev) break;
+  if (i < g_attr.used && g_attr.smem[i] >= smem) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (i == g_attr.used) {
+    if (g_attr.used == AttrCache::kSlots) return cudaSuccess;   // full: just do not cache
+    ++g_attr.used;
+    g_attr.fn[i] = fn;
+    g_attr.device[i] = dev;
+  }
+  g_attr.smem[i] = smem;
+  return cudaSuccess;
+}
+
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem);
+  cudaError_t e = ensure_smem_attr(fn, ls.smem);
   if (e != cudaSuccess) return e;
   void* args[] = {params};
   e = cudaLaunchKernel(fn, dim3(ls.grid), dim3(ls.threads), args, ls.smem, st);
@@ -858,12 +967,16 @@ sp_status_t sp_debug_inject(sp_status_t code) {
   return SP_OK;
 }
 
-sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm) {
+sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm,
+                          int32_t threads, int32_t chunks) {
   if (kernel < 0 || kernel > 1 || stages < 0 || stages > 8 || blocks_per_sm < 0 ||
-      blocks_per_sm > 8)
+      blocks_per_sm > 16 || threads < 0 || threads > 1024 || chunks < 0 || chunks > 8)
     return fail(SP_ERR_INVALID_ARG, "sp_debug_tune: bad arguments");
   g_tune[kernel][0].store(stages);
   g_tune[kernel][1].store(blocks_per_sm);
+  g_tune[kernel][2].store(threads);
+  g_tune[kernel][3].store(chunks);
+  g_tune_epoch.fetch_add(1);   // cached launch shapes are stale now
   return SP_OK;
 }
 
