@@ -138,6 +138,48 @@ constexpr size_t kSmemPerSm = 228 * 1024;     // sm_100-class shared memory per 
 constexpr size_t kSmemPerBlock = 227 * 1024;  // opt-in maximum per block
 constexpr size_t kReserve = 1024;             // per-block reservation
 
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  return dev;
+}
+
+// The dynamic shared-memory opt-in of each kernel, per (kernel, device): it is
+// only ever raised, to the largest size requested so far, and every setter
+// goes through here so the cache always matches the driver's value.
+struct AttrCache {
+  std::mutex mu;
+  static constexpr int kSlots = 256;
+  const void* fn[kSlots];
+  int device[kSlots];
+  size_t smem[kSlots];
+  int used = 0;
+};
+AttrCache g_attr;
+
+cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_attr.mu);
+  int i = 0;
+  for (; i < g_attr.used; ++i)
+    if (g_attr.fn[i] == fn && g_attr.device[i] == dev) break;
+  if (i < g_attr.used && g_attr.smem[i] >= smem) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (i == g_attr.used) {
+    if (g_attr.used == AttrCache::kSlots) return cudaSuccess;   // full: just do not cache
+    ++g_attr.used;
+    g_attr.fn[i] = fn;
+    g_attr.device[i] = dev;
+  }
+  g_attr.smem[i] = smem;
+  return cudaSuccess;
+}
+
 // Launch shapes are pure functions of (kernel kind, rows, h, t, flags, device,
 // tuning overrides); caching them keeps the per-call host cost to the
 // argument checks, which matters for short kernels.
@@ -160,15 +202,6 @@ struct ShapeCache {
 
 ShapeCache g_shapes;
 std::atomic<int> g_tune_epoch{0};
-
-int current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    dev = -1;
-  }
-  return dev;
-}
 
 template <typename Make>
 LaunchShape cached_shape(int kind, int64_t rows, int64_t h, int t, int flags, Make make) {
@@ -224,9 +257,7 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
   ls.smem = stages * unit_bytes + fixed_bytes;
   const void* fn = kernel_of(stages);
   int occ = bps;
-  if (fn != nullptr &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem) ==
-          cudaSuccess) {
+  if (fn != nullptr && ensure_smem_attr(fn, ls.smem) == cudaSuccess) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, ls.threads, ls.smem) ==
             cudaSuccess &&
@@ -366,38 +397,6 @@ LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
 LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
   return cached_shape(3, rows, h, 0, (has_skip ? 1 : 0) | (regen ? 2 : 0),
                       [&] { return bwd_shape_uncached(rows, h, has_skip, regen); });
-}
-
-// The dynamic shared-memory opt-in of each kernel, set once per (kernel,
-// device) to the largest size requested so far.
-struct AttrCache {
-  std::mutex mu;
-  static constexpr int kSlots = 256;
-  const void* fn[kSlots];
-  int device[kSlots];
-  size_t smem[kSlots];
-  int used = 0;
-};
-AttrCache g_attr;
-
-cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
-  const int dev = current_device();
-  std::lock_guard<std::mutex> lock(g_attr.mu);
-  int i = 0;
-  for (; i < g_attr.used; ++i)
-    if (g_attr.fn[i] == fn && g_attr.device[i] == dev) break;
-  if (i < g_attr.used && g_attr.smem[i] >= smem) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (i == g_attr.used) {
-    if (g_attr.used == AttrCache::kSlots) return cudaSuccess;   // full: just do not cache
-    ++g_attr.used;
-    g_attr.fn[i] = fn;
-    g_attr.device[i] = dev;
-  }
-  g_attr.smem[i] = smem;
-  return cudaSuccess;
 }
 
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {

@@ -581,3 +581,14 @@ def test_rs_norm_bwd_equals_unfused_reduce_then_norm_bwd_within_rounding():
     torch.cuda.synchronize()
     for a, b in zip(fused["dres"] + fused["dgat"], plain["dres"] + plain["dgat"]):
         assert np.array_equal(compare.bf16_bits(a), compare.bf16_bits(b))
+
+
+def test_one_kernel_across_shared_memory_sizes():
+    """The same kernel instantiation (run-time t) needs more shared memory for
+    more ranks; calls with large, small, then medium needs must all launch."""
+    for t in (16, 2, 5, 3, 16):
+        w = wl.Workload("sm", t=t, b=1, s=16 * t, h=512, draw_seed=90 + t)
+        inp = wl.forward_inputs(w, C.DEV)
+        out = C.run_fwd(w, inp)
+        torch.cuda.synchronize()
+        C.check_fwd_rows(w, inp, out, C.sample_tokens(w, 8))
