@@ -30,6 +30,9 @@ sp_status_t fail(sp_status_t code, const char* fmt, ...) {
 }
 
 sp_status_t fail_cuda(cudaError_t e, const char* where) {
+  if (e == cudaErrorInvalidConfiguration)
+    return fail(SP_ERR_UNSUPPORTED, "%s: no launch shape of this kernel fits the shared memory "
+                "of one SM for these sizes", where);
   return fail(SP_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
@@ -253,6 +256,7 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
     stages = opts[n_opts - 1];
     bps = 1;
   }
+  ls.fits = ok;
   ls.stages = stages;
   ls.smem = stages * unit_bytes + fixed_bytes;
   const void* fn = kernel_of(stages);
@@ -272,7 +276,7 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
 }
 
 const int kFwdStages[] = {3, 2};
-const int kBwdRing[] = {3, 2};
+const int kBwdRing[] = {3, 2, 1};   // row pairs; 1 = no prefetch (very wide rows)
 
 // Forward threads per block: the largest of 256, 160, 128, 64 that splits the
 // row's h/8 vectors into at least 4 (else at least 2) full chunks, so no
@@ -374,7 +378,7 @@ LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool rege
   const size_t item =
       static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
   const size_t ring_pair = 2 * item * maxc;   // rows are staged two at a time
-  return pick_shape(1, threads, maxc, rows, ring_pair, 2 * 32 * sizeof(float4), kBwdRing, 2,
+  return pick_shape(1, threads, maxc, rows, ring_pair, 2 * 32 * sizeof(float4), kBwdRing, 3,
                     /*ring=*/2, /*blocks per SM=*/threads <= 256 ? 512 / threads : 1, [&](int st) {
                       return regen ? bwd_regen_kernel(threads, maxc, st)
                                    : bwd_kernel(threads, maxc, st);
@@ -401,6 +405,7 @@ LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false
 
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
+  if (!ls.fits) return cudaErrorInvalidConfiguration;   // reported as SP_ERR_UNSUPPORTED
   cudaError_t e = ensure_smem_attr(fn, ls.smem);
   if (e != cudaSuccess) return e;
   void* args[] = {params};

@@ -8,6 +8,7 @@ namespace spb {
 template <int NTHR, int MAXC, bool REGEN>
 static const void* bwd_kernel_s(int ring) {
   switch (ring) {
+    case 1: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 1, REGEN>);
     case 2: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 2, REGEN>);
     case 3: return reinterpret_cast<const void*>(norm_bwd_kernel<NTHR, MAXC, 3, REGEN>);
     default: return nullptr;
@@ -15,7 +16,7 @@ static const void* bwd_kernel_s(int ring) {
 }
 
 // Instantiated shapes (threads, chunks per row): (64, 1), (128, 2), (256, 1),
-// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1); ring of 2 or 3 rows.
+// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1); ring of 1, 2 or 3 row pairs.
 template <bool REGEN>
 static const void* bwd_kernel_any(int threads, int maxc, int ring) {
   switch (threads * 8 + maxc) {

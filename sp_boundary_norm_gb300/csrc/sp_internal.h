@@ -91,6 +91,7 @@ struct LaunchShape {
   int stages;      // cp.async pipeline depth (forward: chunks; backward: rows)
   int grid;        // blocks
   size_t smem;     // dynamic shared memory bytes
+  bool fits;       // false: no instantiated shape fits this SM's shared memory
 };
 
 int device_sm_count();
