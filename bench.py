@@ -33,8 +33,8 @@ from sp_boundary_norm_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "SP-boundary fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak) at h=8192,t=8"
 UNIT = "tokens/s"
-FWD_SOURCES = ("sp_boundary_norm_gb300/csrc/fwd.cu", "sp_boundary_norm_gb300/csrc/sp_device.cuh",
-               "sp_boundary_norm_gb300/csrc/sp_internal.h")
+FWD_SOURCES = ("sp_boundary_norm_gb300/csrc/fwd.cu", "sp_boundary_norm_gb300/csrc/fwd_kernel.cuh",
+               "sp_boundary_norm_gb300/csrc/sp_device.cuh", "sp_boundary_norm_gb300/csrc/sp_internal.h")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "rs_norm_fwd_kernel_70b.md")
 
 

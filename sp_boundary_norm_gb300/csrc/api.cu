@@ -276,7 +276,7 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
 }
 
 const int kFwdStages[] = {3, 2};
-const int kBwdRing[] = {3, 2, 1};   // row pairs; 1 = no prefetch (very wide rows)
+const int kBwdRing[] = {3, 2, 1};   // rows staged; 1 = no prefetch (very wide rows)
 
 // Forward threads per block: the largest of 256, 160, 128, 64 that splits the
 // row's h/8 vectors into at least 4 (else at least 2) full chunks, so no
@@ -377,8 +377,8 @@ LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool rege
   bwd_threads(h, &threads, &maxc);
   const size_t item =
       static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
-  const size_t ring_pair = 2 * item * maxc;   // rows are staged two at a time
-  return pick_shape(1, threads, maxc, rows, ring_pair, 2 * 32 * sizeof(float4), kBwdRing, 3,
+  const size_t ring_row = item * maxc;
+  return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 3,
                     /*ring=*/2, /*blocks per SM=*/threads <= 256 ? 512 / threads : 1, [&](int st) {
                       return regen ? bwd_regen_kernel(threads, maxc, st)
                                    : bwd_kernel(threads, maxc, st);

@@ -16,7 +16,7 @@ static const void* bwd_kernel_s(int ring) {
 }
 
 // Instantiated shapes (threads, chunks per row): (64, 1), (128, 2), (256, 1),
-// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1); ring of 1, 2 or 3 row pairs.
+// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1); ring of 1, 2 or 3 rows.
 template <bool REGEN>
 static const void* bwd_kernel_any(int threads, int maxc, int ring) {
   switch (threads * 8 + maxc) {

@@ -9,12 +9,6 @@ namespace spb {
 // REGEN = true: the mask-free variant; the dropout keep decisions are drawn
 // again from Philox4x32-10 at the element's global index (the forward's seed
 // and offset) instead of being read from the stored 1-byte mask.
-//
-// A block takes its rows two at a time: both rows are staged by one cp.async
-// group, their four row sums are reduced together behind one barrier, and
-// the per-row bookkeeping (cursors, addresses, statistics) is shared, while
-// each thread gets two independent rows of arithmetic to interleave.  RING is
-// the number of row pairs held in shared memory (RING - 1 pairs ahead).
 template <int NTHR, int MAXC, int RING, bool REGEN>
 __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
     norm_bwd_kernel(const BwdParams P) {
@@ -32,8 +26,7 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
   constexpr int off_skip = off_mask + (REGEN ? 0 : NTHR * 8);
   const int item_bytes = off_skip + (has_skip ? v16 : 0);
   const int row_bytes = MAXC * item_bytes;
-  const int pair_bytes = 2 * row_bytes;
-  float4* red = reinterpret_cast<float4*>(smem + RING * pair_bytes);   // [2][32]
+  float2* red = reinterpret_cast<float2*>(smem + RING * row_bytes);   // [2][32]
   const int c0 = tid * 8;
   uint32_t valid = 0;   // bit ch: this thread has channels in chunk ch
 #pragma unroll
@@ -44,7 +37,6 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
 
   const int64_t G = gridDim.x;
   const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
-  const int64_t npairs = (nrows + 1) / 2;
 
   // gamma of this thread's channels, kept for every row
   uint4 gam[MAXC];
@@ -52,42 +44,38 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
   for (int ch = 0; ch < MAXC; ++ch)
     gam[ch] = ((valid >> ch) & 1u) ? ldg16(P.gamma + ch * kChunk + c0) : make_uint4(0, 0, 0, 0);
 
-  // ---- staging: the next pair of rows into the next ring slot -----------
+  // Stage the next row (all of its chunks, one cp.async group) into the next
+  // ring slot; rows are issued in order, so one cursor walks them.
   RowCursor pf;
   pf.init(P.map, blockIdx.x);
   int64_t pf_ri = 0;
   int pf_slot = 0;
-  auto stage_row = [&](uint8_t* it0) {   // it0: this thread's slot in the row's first item
-    const int k = pf.k;
-    const int64_t lo0 = pf.local(P.map) * h + c0;
-    const uint16_t* dyp = P.dy[k] + lo0;
-    const uint16_t* zp = P.z[k] + lo0;
+  auto issue_row = [&]() {
+    if (pf_ri < nrows) {
+      const int k = pf.k;
+      const int64_t lo0 = pf.local(P.map) * h + c0;
+      const uint16_t* dyp = P.dy[k] + lo0;
+      const uint16_t* zp = P.z[k] + lo0;
+      const uint8_t* mp = REGEN ? nullptr : P.mask[k] + lo0;
+      uint8_t* it0 = smem + pf_slot * row_bytes + tid * 16;
 #pragma unroll
-    for (int ch = 0; ch < MAXC; ++ch) {
-      if ((valid >> ch) & 1u) {
-        uint8_t* it = it0 + ch * item_bytes;
-        cp_async16(it, dyp + ch * kChunk);
-        cp_async16(it + v16, zp + ch * kChunk);
-        if (!REGEN) cp_async8(it + off_mask - tid * 8, P.mask[k] + lo0 + ch * kChunk);
-        if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
+      for (int ch = 0; ch < MAXC; ++ch) {
+        if ((valid >> ch) & 1u) {
+          uint8_t* it = it0 + ch * item_bytes;
+          cp_async16(it, dyp + ch * kChunk);
+          cp_async16(it + v16, zp + ch * kChunk);
+          if (!REGEN) cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // 8 B apart
+          if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
+        }
       }
-    }
-  };
-  auto issue_pair = [&]() {
-    uint8_t* pb = smem + pf_slot * pair_bytes + tid * 16;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      if (pf_ri < nrows) {
-        stage_row(pb + q * row_bytes);
-        if (++pf_ri < nrows) pf.advance(P.map, G);
-      }
+      if (++pf_ri < nrows) pf.advance(P.map, G);
     }
     cp_async_commit();
     pf_slot = (pf_slot + 1 == RING) ? 0 : pf_slot + 1;
   };
 
 #pragma unroll
-  for (int i = 0; i < RING - 1; ++i) issue_pair();
+  for (int i = 0; i < RING - 1; ++i) issue_row();
 
   float acc_g[MAXC][8], acc_b[MAXC][8], acc_bias[MAXC][8];
 #pragma unroll
@@ -95,11 +83,43 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc_g[ch][e] = acc_b[ch][e] = acc_bias[ch][e] = 0.f;
 
-  // ---- per-row passes ----------------------------------------------------
-  // pass 1: the two row sums of one row, and its dgamma / dbeta terms;
-  // x_hat = (z - mean) * rstd (LN) or z * rstd (RMS); dxh = dY * gamma is an
-  // exact product of two bf16 values.
-  auto pass1 = [&](const uint8_t* it0, float nmean, float rstd, float& s1, float& s2) {
+  // statistics of the current row, loaded one row ahead
+  RowCursor cur, nxt;
+  cur.init(P.map, blockIdx.x);
+  nxt = cur;
+  float cur_mean = 0.f, cur_rstd = 0.f;
+  if (nrows > 0) {
+    const int64_t l0 = cur.local(P.map);
+    cur_rstd = P.rstd[cur.k][l0];
+    if (is_ln) cur_mean = P.mean[cur.k][l0];
+  }
+
+  int slot_sel = 0;
+  int slot = 0;   // ring slot of the current row
+  const float fh = static_cast<float>(h);
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    if (ri > 0) cur = nxt;
+    const int64_t row = cur.row;
+    const int k = cur.k;
+    const int64_t local = cur.local(P.map);
+    float nx_mean = 0.f, nx_rstd = 0.f;
+    if (ri + 1 < nrows) {
+      nxt.advance(P.map, G);
+      const int64_t l1 = nxt.local(P.map);
+      nx_rstd = P.rstd[nxt.k][l1];
+      if (is_ln) nx_mean = P.mean[nxt.k][l1];
+    }
+    const float mean = cur_mean, rstd = cur_rstd;
+
+    issue_row();                    // row ri + RING - 1 refills the slot row ri - 1 used
+    cp_async_wait<RING - 1>();      // row ri has landed
+    const uint8_t* it0 = smem + slot * row_bytes + tid * 16;
+    slot = (slot + 1 == RING) ? 0 : slot + 1;
+
+    // ---- pass 1: the two row sums, and dgamma / dbeta terms --------------
+    // x_hat = (z - mean) * rstd (LN) or z * rstd (RMS); dxh = dY * gamma is an
+    // exact product of two bf16 values
+    const float nmean = is_ln ? -mean : 0.f;
     float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
@@ -121,15 +141,16 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
         }
       }
     }
-    s1 = s1a + s1b;
-    s2 = s2a + s2b;
-  };
-  // pass 2: dZ = rstd * (dxh - m1 - (z - mean) * rstd * m2), dResidual,
-  // dYpre (gathered), dbias terms.
-  auto pass2 = [&](const uint8_t* it0, float nmean, float rstd, float nm1, float nm2r,
-                   const RowCursor& rc) {
-    uint16_t* dres_row = P.dresidual[rc.k] + rc.local(P.map) * h + c0;
-    const int64_t grow = rc.row * h + c0;
+
+    const float2 s = block_sum2(s1a + s1b, s2a + s2b, red + 32 * slot_sel);
+    slot_sel ^= 1;
+    const float nm1 = is_ln ? -(s.x / fh) : 0.f;
+    const float nm2r = -(s.y / fh) * rstd;
+
+    // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
+    // dZ = rstd * (dxh - m1 - (z - mean) * rstd * m2)
+    uint16_t* dres_row = P.dresidual[k] + local * h + c0;
+    const int64_t grow = row * h + c0;
     uint16_t* dg0_row = P.n_gather > 0 ? P.dgathered[0] + grow : nullptr;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
@@ -149,7 +170,7 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
                                         P.key0, P.key1);
           mk = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         } else {
-          mk = lds8(it + off_mask - tid * 8);   // mask slots are 8 B apart
+          mk = lds8(it + off_mask - tid * 8);
         }
         float zc[8], dz[8], dp[8];
         add8_bf16_bcast(zv, nmean, zc);           // z - mean
@@ -176,63 +197,8 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
         for (int j = 1; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
       }
     }
-  };
-
-  // statistics of the current pair's rows, loaded one pair ahead
-  RowCursor ca, cb;   // the current pair's rows
-  ca.init(P.map, blockIdx.x);
-  cb = ca;
-  if (nrows > 1) cb.advance(P.map, G);
-  RowCursor na = ca, nb = cb;   // the next pair's rows (for the statistics)
-  auto load_stats = [&](const RowCursor& c, float& mean, float& rstd) {
-    const int64_t l = c.local(P.map);
-    rstd = P.rstd[c.k][l];
-    mean = is_ln ? P.mean[c.k][l] : 0.f;
-  };
-  float mean_a = 0.f, rstd_a = 0.f, mean_b = 0.f, rstd_b = 0.f;
-  if (nrows > 0) load_stats(ca, mean_a, rstd_a);
-  if (nrows > 1) load_stats(cb, mean_b, rstd_b);
-
-  int slot_sel = 0;
-  int slot = 0;   // ring slot of the current pair
-  const float fh = static_cast<float>(h);
-  for (int64_t pi = 0; pi < npairs; ++pi) {
-    const bool has_b = 2 * pi + 1 < nrows;
-    if (pi > 0) {
-      ca = na;
-      cb = nb;
-    }
-    float nx_mean_a = 0.f, nx_rstd_a = 0.f, nx_mean_b = 0.f, nx_rstd_b = 0.f;
-    if (2 * pi + 2 < nrows) {
-      na = cb;
-      na.advance(P.map, G);
-      load_stats(na, nx_mean_a, nx_rstd_a);
-      if (2 * pi + 3 < nrows) {
-        nb = na;
-        nb.advance(P.map, G);
-        load_stats(nb, nx_mean_b, nx_rstd_b);
-      }
-    }
-
-    issue_pair();                   // pair pi + RING - 1 refills the slot pair pi - 1 used
-    cp_async_wait<RING - 1>();      // pair pi has landed
-    const uint8_t* pa = smem + slot * pair_bytes + tid * 16;
-    const uint8_t* pbk = pa + row_bytes;
-    slot = (slot + 1 == RING) ? 0 : slot + 1;
-
-    const float nmean_a = is_ln ? -mean_a : 0.f, nmean_b = is_ln ? -mean_b : 0.f;
-    float4 sums = make_float4(0.f, 0.f, 0.f, 0.f);
-    pass1(pa, nmean_a, rstd_a, sums.x, sums.y);
-    if (has_b) pass1(pbk, nmean_b, rstd_b, sums.z, sums.w);
-    const float4 tot = block_sum4(sums, red + 32 * slot_sel);
-    slot_sel ^= 1;
-    pass2(pa, nmean_a, rstd_a, is_ln ? -(tot.x / fh) : 0.f, -(tot.y / fh) * rstd_a, ca);
-    if (has_b) pass2(pbk, nmean_b, rstd_b, is_ln ? -(tot.z / fh) : 0.f, -(tot.w / fh) * rstd_b, cb);
-
-    mean_a = nx_mean_a;
-    rstd_a = nx_rstd_a;
-    mean_b = nx_mean_b;
-    rstd_b = nx_rstd_b;
+    cur_mean = nx_mean;
+    cur_rstd = nx_rstd;
   }
   cp_async_wait<0>();
 

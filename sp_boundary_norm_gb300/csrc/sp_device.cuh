@@ -335,15 +335,6 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
   return make_float2(warp_sum(p.x), warp_sum(p.y));
 }
 
-__device__ __forceinline__ float4 block_sum4(float4 v, float4* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = make_float4(warp_sum(v.x), warp_sum(v.y), warp_sum(v.z), warp_sum(v.w));
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  const float4 p = lane < nw ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-  return make_float4(warp_sum(p.x), warp_sum(p.y), warp_sum(p.z), warp_sum(p.w));
-}
-
 // ------------------------------------------------------------- shard map --
 // Position of token `row` = bi*s + si of the (b, s) grid: its shard k (the
 // shard holding positions [o_k, o_{k+1}) of each batch row) and its row index
