@@ -35,8 +35,9 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
-  const int64_t G = gridDim.x;
-  const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
+  // this block's rows: a contiguous range
+  int64_t r0, nrows;
+  block_rows(P.rows, blockIdx.x, gridDim.x, &r0, &nrows);
 
   // gamma of this thread's channels, kept for every row
   uint4 gam[MAXC];
@@ -45,15 +46,21 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
     gam[ch] = ((valid >> ch) & 1u) ? ldg16(P.gamma + ch * kChunk + c0) : make_uint4(0, 0, 0, 0);
 
   // Stage the next row (all of its chunks, one cp.async group) into the next
-  // ring slot; rows are issued in order, so one cursor walks them.
-  RowCursor pf;
-  pf.init(P.map, blockIdx.x);
+  // ring slot and load its statistics; the row's shard, position and
+  // statistics travel with it in a register queue of RING - 1 entries.
+  struct RowRec {
+    int64_t row, local;
+    int k;
+    float mean, rstd;
+  };
+  RowWalk pw;
+  pw.init(P.map, r0);
   int64_t pf_ri = 0;
   int pf_slot = 0;
-  auto issue_row = [&]() {
+  auto issue_row = [&](RowRec& rec) {
     if (pf_ri < nrows) {
-      const int k = pf.k;
-      const int64_t lo0 = pf.local(P.map) * h + c0;
+      const int k = pw.k;
+      const int64_t lo0 = pw.local * h + c0;
       const uint16_t* dyp = P.dy[k] + lo0;
       const uint16_t* zp = P.z[k] + lo0;
       const uint8_t* mp = REGEN ? nullptr : P.mask[k] + lo0;
@@ -68,14 +75,21 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
           if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
         }
       }
-      if (++pf_ri < nrows) pf.advance(P.map, G);
+      rec.row = pw.row;
+      rec.local = pw.local;
+      rec.k = k;
+      rec.rstd = __ldg(P.rstd[k] + pw.local);
+      rec.mean = is_ln ? __ldg(P.mean[k] + pw.local) : 0.f;
+      if (++pf_ri < nrows) pw.next(P.map);
     }
     cp_async_commit();
     pf_slot = (pf_slot + 1 == RING) ? 0 : pf_slot + 1;
   };
 
+  constexpr int kQ = RING > 1 ? RING - 1 : 1;
+  RowRec q[kQ];
 #pragma unroll
-  for (int i = 0; i < RING - 1; ++i) issue_row();
+  for (int i = 0; i < RING - 1; ++i) issue_row(q[i]);
 
   float acc_g[MAXC][8], acc_b[MAXC][8], acc_bias[MAXC][8];
 #pragma unroll
@@ -83,36 +97,25 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc_g[ch][e] = acc_b[ch][e] = acc_bias[ch][e] = 0.f;
 
-  // statistics of the current row, loaded one row ahead
-  RowCursor cur, nxt;
-  cur.init(P.map, blockIdx.x);
-  nxt = cur;
-  float cur_mean = 0.f, cur_rstd = 0.f;
-  if (nrows > 0) {
-    const int64_t l0 = cur.local(P.map);
-    cur_rstd = P.rstd[cur.k][l0];
-    if (is_ln) cur_mean = P.mean[cur.k][l0];
-  }
-
   int slot_sel = 0;
   int slot = 0;   // ring slot of the current row
-  const float fh = static_cast<float>(h);
+  const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
-    if (ri > 0) cur = nxt;
+    // row ri + RING - 1 refills the slot row ri - 1 used
+    RowRec cur;
+    if (RING > 1) {
+      cur = q[0];
+#pragma unroll
+      for (int i = 0; i + 1 < kQ; ++i) q[i] = q[i + 1];
+      issue_row(q[kQ - 1]);
+    } else {
+      issue_row(cur);
+    }
+    cp_async_wait<RING - 1>();      // row ri has landed
     const int64_t row = cur.row;
     const int k = cur.k;
-    const int64_t local = cur.local(P.map);
-    float nx_mean = 0.f, nx_rstd = 0.f;
-    if (ri + 1 < nrows) {
-      nxt.advance(P.map, G);
-      const int64_t l1 = nxt.local(P.map);
-      nx_rstd = P.rstd[nxt.k][l1];
-      if (is_ln) nx_mean = P.mean[nxt.k][l1];
-    }
-    const float mean = cur_mean, rstd = cur_rstd;
-
-    issue_row();                    // row ri + RING - 1 refills the slot row ri - 1 used
-    cp_async_wait<RING - 1>();      // row ri has landed
+    const int64_t local = cur.local;
+    const float mean = cur.mean, rstd = cur.rstd;
     const uint8_t* it0 = smem + slot * row_bytes + tid * 16;
     slot = (slot + 1 == RING) ? 0 : slot + 1;
 
@@ -144,8 +147,8 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
 
     const float2 s = block_sum2(s1a + s1b, s2a + s2b, red + 32 * slot_sel);
     slot_sel ^= 1;
-    const float nm1 = is_ln ? -(s.x / fh) : 0.f;
-    const float nm2r = -(s.y / fh) * rstd;
+    const float nm1 = is_ln ? -(s.x * inv_h) : 0.f;
+    const float nm2r = -(s.y * inv_h) * rstd;
 
     // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
     // dZ = rstd * (dxh - m1 - (z - mean) * rstd * m2)
@@ -197,8 +200,6 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
         for (int j = 1; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
       }
     }
-    cur_mean = nx_mean;
-    cur_rstd = nx_rstd;
   }
   cp_async_wait<0>();
 

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
   }
 
   int stage = 0, buf = 0, slot_sel = 0;
-  const float fh = static_cast<float>(h);
+  const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
     if (ri > 0) cur = nxt;
     const int64_t row = cur.row;
@@ -172,8 +172,8 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
 
     const float2 s = block_sum2(s1a + s1b, s2a + s2b, red + 32 * slot_sel);
     slot_sel ^= 1;
-    const float nm1 = is_ln ? -(s.x / fh) : 0.f;
-    const float nm2r = -(s.y / fh) * rstd;
+    const float nm1 = is_ln ? -(s.x * inv_h) : 0.f;
+    const float nm2r = -(s.y * inv_h) * rstd;
 
     // ---- pass 2: dZ, dResidual, dYpre (gathered), dbias terms ------------
     uint16_t* dres_row = P.dresidual[k] + local * h + c0;

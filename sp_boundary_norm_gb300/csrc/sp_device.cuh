@@ -371,6 +371,49 @@ struct RowCursor {
   }
 };
 
+// The rows of one block as a contiguous range r0, r0 + 1, ...: the walk
+// steps one token at a time, so the shard index, the row inside the shard and
+// the shard's end position change by increments; the shard search runs only
+// when a step reaches the end of a shard or of a batch row.
+struct RowWalk {
+  int64_t row, bi, si, local, end;
+  int k;
+
+  __device__ __forceinline__ void locate(const ShardMap& m) {
+    while (k + 1 < m.t && m.off[k + 1] <= si) ++k;   // skips empty shards
+    local = bi * (m.off[k + 1] - m.off[k]) + (si - m.off[k]);
+    end = m.off[k + 1];
+  }
+  __device__ __forceinline__ void init(const ShardMap& m, int64_t r) {
+    row = r;
+    bi = (m.b > 1 && m.s > 0) ? r / m.s : 0;
+    si = r - bi * m.s;
+    k = 0;
+    locate(m);
+  }
+  __device__ __forceinline__ void next(const ShardMap& m) {
+    ++row;
+    ++local;
+    if (++si == end) {
+      if (si == m.s) {
+        ++bi;
+        si = 0;
+        k = 0;
+      }
+      locate(m);
+    }
+  }
+};
+
+// First row and row count of block `blk` of `nblk` when `rows` rows are cut
+// into contiguous ranges whose sizes differ by at most one.
+__device__ __forceinline__ void block_rows(int64_t rows, int64_t blk, int64_t nblk, int64_t* r0,
+                                           int64_t* n) {
+  const int64_t a = rows * blk / nblk, b = rows * (blk + 1) / nblk;
+  *r0 = a;
+  *n = b - a;
+}
+
 // Device check of packed-sequence metadata: cu_seqlens[0] == 0, non-decreasing,
 // cu_seqlens[n] == total.  Run by one warp; flags SP_ERR_DEVICE_CHECK.
 __device__ __forceinline__ void check_cu_seqlens(const int32_t* cu, int32_t n, int64_t total,
