@@ -7,12 +7,13 @@
 // rank's row-linear partial entered the sum with weight one, so each receives
 // the full-sequence gradient of the pre-dropout sum, dYpre.
 //
-// Work layout mirrors the forward: a persistent grid, one token row per block
-// iteration, chunks of 8*T channels with thread i owning channels
+// Work layout mirrors the forward: a persistent grid, a contiguous range of
+// token rows per block, chunks of 8*T channels with thread i owning channels
 // [8i, 8i+8) of each chunk.  Each thread stages its own pieces of dY, Z, the
 // mask (and the optional skip-path gradient) of whole rows with cp.async into
-// a ring of RING rows in shared memory, RING - 1 rows ahead; the two passes a
-// row needs (the row sums mean(dxh) and mean(dxh * x_hat), then the
+// a ring of RING rows in shared memory, RING - 1 rows ahead; the row's
+// statistics are loaded when it is staged and wait in registers.  The two
+// passes a row needs (the row sums mean(dxh) and mean(dxh * x_hat), then the
 // gradients) both read the row from there.  The two sums are reduced
 // together: one block barrier per row.  Because a thread owns the same
 // channels in every row, it accumulates its channels' parameter-gradient

@@ -32,16 +32,17 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
-  const int64_t G = gridDim.x;
-  const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
+  // this block's rows: a contiguous range
+  int64_t r0, nrows;
+  block_rows(P.rows, blockIdx.x, gridDim.x, &r0, &nrows);
   const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
 
   // ---- prefetch cursor: the next (row, chunk) item to stage -------------
   // pf_goff: element offset of (row, chunk) in the (b, s, h) partials;
   // pf_roff: element offset in the residual shard of that row.
-  RowCursor pf;
-  pf.init(P.map, blockIdx.x);
-  int64_t pf_ri = 0, pf_goff = pf.row * h + c0, pf_roff = pf.local(P.map) * h + c0;
+  RowWalk pf;
+  pf.init(P.map, r0);
+  int64_t pf_ri = 0, pf_goff = pf.row * h + c0, pf_roff = pf.local * h + c0;
   int pf_chunk = 0, pf_stage = 0;
 
   auto issue_next = [&]() {
@@ -60,9 +61,9 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
       if (++pf_chunk == nchunk) {
         pf_chunk = 0;
         if (++pf_ri < nrows) {
-          pf.advance(P.map, G);
+          pf.next(P.map);
           pf_goff = pf.row * h + c0;
-          pf_roff = pf.local(P.map) * h + c0;
+          pf_roff = pf.local * h + c0;
         }
       } else {
         pf_goff += kChunk;
@@ -76,16 +77,16 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
 #pragma unroll
   for (int i = 0; i < STAGES - 1; ++i) issue_next();
 
-  RowCursor cur;
-  cur.init(P.map, blockIdx.x);
+  RowWalk cur;
+  cur.init(P.map, r0);
   int stage = 0;
   int slot_sel = 0;
-  const float fh = static_cast<float>(h);
+  const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
-    if (ri > 0) cur.advance(P.map, G);
+    if (ri > 0) cur.next(P.map);
     const int64_t row = cur.row;
     const int k = cur.k;
-    const int64_t local = cur.local(P.map);
+    const int64_t local = cur.local;
     uint16_t* zrow = P.z[k] + local * h + c0;
     uint8_t* mrow = P.mask[k] + local * h + c0;
     const uint64_t e_row = static_cast<uint64_t>(row * h + c0);   // global element index
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
     // ---- token-wise statistics over h ------------------------------------
     float mean = 0.f, rstd;
     if (is_ln) {
-      mean = block_sum(lsum, red + 32 * slot_sel) / fh;
+      mean = block_sum(lsum, red + 32 * slot_sel) * inv_h;
       slot_sel ^= 1;
       float lsqa = 0.f, lsqb = 0.f;
       const float nmean = -mean;
@@ -169,11 +170,11 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
           for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
         }
       }
-      const float var = block_sum(lsqa + lsqb, red + 32 * slot_sel) / fh;
+      const float var = block_sum(lsqa + lsqb, red + 32 * slot_sel) * inv_h;
       slot_sel ^= 1;
       rstd = rsqrtf(var + P.eps);
     } else {
-      const float ms = block_sum(lsum, red + 32 * slot_sel) / fh;
+      const float ms = block_sum(lsum, red + 32 * slot_sel) * inv_h;
       slot_sel ^= 1;
       rstd = rsqrtf(ms + P.eps);
     }

@@ -47,8 +47,9 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
-  const int64_t G = gridDim.x;
-  const int64_t nrows = (P.rows > blockIdx.x) ? (P.rows - 1 - blockIdx.x) / G + 1 : 0;
+  // this block's rows: a contiguous range
+  int64_t r0, nrows;
+  block_rows(P.rows, blockIdx.x, gridDim.x, &r0, &nrows);
 
   uint4 gam[MAXC];
 #pragma unroll
@@ -57,8 +58,8 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
 
   // ---- prefetch cursor over (row, chunk) items ---------------------------
   // P.dy[r] holds rank r's full (b, s, h) partial gradient here.
-  RowCursor pf;
-  pf.init(P.map, blockIdx.x);
+  RowWalk pf;
+  pf.init(P.map, r0);
   int64_t pf_ri = 0;
   int pf_chunk = 0, pf_stage = 0, pf_buf = 0;
   auto issue_next = [&]() {
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
       if (pf_chunk == 0) {
         // the row's Z, mask (and skip gradient), all chunks, ride with chunk 0
         const int k = pf.k;
-        const int64_t lo0 = pf.local(P.map) * h + c0;
+        const int64_t lo0 = pf.local * h + c0;
         uint8_t* rb = rowbuf + pf_buf * MAXC * rb_item + tid * 16;
 #pragma unroll
         for (int ch = 0; ch < MAXC; ++ch) {
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
       }
       if (++pf_chunk == nchunk) {
         pf_chunk = 0;
-        if (++pf_ri < nrows) pf.advance(P.map, G);
+        if (++pf_ri < nrows) pf.next(P.map);
       }
     }
     cp_async_commit();
@@ -104,12 +105,12 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc_g[ch][e] = acc_b[ch][e] = acc_bias[ch][e] = 0.f;
 
-  RowCursor cur, nxt;
-  cur.init(P.map, blockIdx.x);
+  RowWalk cur, nxt;
+  cur.init(P.map, r0);
   nxt = cur;
   float cur_mean = 0.f, cur_rstd = 0.f;
   if (nrows > 0) {
-    const int64_t l0 = cur.local(P.map);
+    const int64_t l0 = cur.local;
     cur_rstd = P.rstd[cur.k][l0];
     if (is_ln) cur_mean = P.mean[cur.k][l0];
   }
@@ -120,11 +121,11 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
     if (ri > 0) cur = nxt;
     const int64_t row = cur.row;
     const int k = cur.k;
-    const int64_t local = cur.local(P.map);
+    const int64_t local = cur.local;
     float nx_mean = 0.f, nx_rstd = 0.f;
     if (ri + 1 < nrows) {
-      nxt.advance(P.map, G);
-      const int64_t l1 = nxt.local(P.map);
+      nxt.next(P.map);
+      const int64_t l1 = nxt.local;
       nx_rstd = P.rstd[nxt.k][l1];
       if (is_ln) nx_mean = P.mean[nxt.k][l1];
     }

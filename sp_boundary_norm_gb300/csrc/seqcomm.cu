@@ -5,7 +5,7 @@
 // On one GPU a "rank" is a buffer, so an all-gather is a strided copy of
 // each shard into the full buffer(s) and a reduce-scatter reads shard k's
 // rows from all t partials.  Both are pure HBM streams: a persistent grid,
-// one token row per block iteration, 16-byte loads that bypass L1 and
+// a contiguous range of token rows per block, 16-byte loads that bypass L1 and
 // streaming 16-byte stores, several loads in flight per thread.
 #include "sp_device.cuh"
 
@@ -19,11 +19,14 @@ __global__ void __launch_bounds__(kCopyThreads) allgather_kernel(const CopyParam
     check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
   const int64_t h = P.map.h;
   const int64_t nvec = h / 8;
-  RowCursor cur;
-  cur.init(P.map, blockIdx.x);
-  for (int64_t row = blockIdx.x; row < P.rows; row += gridDim.x) {
-    if (row != blockIdx.x) cur.advance(P.map, gridDim.x);
-    const uint16_t* src = P.src[cur.k] + cur.local(P.map) * h;
+  int64_t r0, nrows;
+  block_rows(P.rows, blockIdx.x, gridDim.x, &r0, &nrows);
+  RowWalk cur;
+  cur.init(P.map, r0);
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    if (ri > 0) cur.next(P.map);
+    const int64_t row = cur.row;
+    const uint16_t* src = P.src[cur.k] + cur.local * h;
     for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += kCopyThreads * kCopyUnroll) {
       uint4 buf[kCopyUnroll];
 #pragma unroll
@@ -48,11 +51,14 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_scatter_kernel(const Copy
     check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
   const int64_t h = P.map.h;
   const int64_t nvec = h / 8;
-  RowCursor cur;
-  cur.init(P.map, blockIdx.x);
-  for (int64_t row = blockIdx.x; row < P.rows; row += gridDim.x) {
-    if (row != blockIdx.x) cur.advance(P.map, gridDim.x);
-    uint16_t* dst = P.dst[cur.k] + cur.local(P.map) * h;
+  int64_t r0, nrows;
+  block_rows(P.rows, blockIdx.x, gridDim.x, &r0, &nrows);
+  RowWalk cur;
+  cur.init(P.map, r0);
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    if (ri > 0) cur.next(P.map);
+    const int64_t row = cur.row;
+    uint16_t* dst = P.dst[cur.k] + cur.local * h;
     for (int64_t v = threadIdx.x; v < nvec; v += kCopyThreads) {
       const int64_t off = row * h + v * 8;
       float y[8], q[8];

@@ -336,41 +336,6 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 }
 
 // ------------------------------------------------------------- shard map --
-// Position of token `row` = bi*s + si of the (b, s) grid: its shard k (the
-// shard holding positions [o_k, o_{k+1}) of each batch row) and its row index
-// inside shard k's (b, s_k) tensor.  A persistent block visits rows
-// r, r + G, r + 2G, ..., so the cursor advances incrementally: the shard index
-// only moves forward within a batch row, and a division happens only when a
-// step crosses into another batch row.
-struct RowCursor {
-  int64_t row, bi, si;
-  int k;
-
-  __device__ __forceinline__ void seek_shard(const ShardMap& m) {
-    while (k + 1 < m.t && m.off[k + 1] <= si) ++k;
-  }
-  __device__ __forceinline__ void init(const ShardMap& m, int64_t r) {
-    row = r;
-    bi = (m.b > 1) ? r / m.s : 0;
-    si = r - bi * m.s;
-    k = 0;
-    seek_shard(m);
-  }
-  __device__ __forceinline__ void advance(const ShardMap& m, int64_t stride) {
-    row += stride;
-    si += stride;
-    if (si >= m.s) {
-      bi += si / m.s;
-      si %= m.s;
-      k = 0;
-    }
-    seek_shard(m);
-  }
-  __device__ __forceinline__ int64_t local(const ShardMap& m) const {
-    return bi * (m.off[k + 1] - m.off[k]) + (si - m.off[k]);
-  }
-};
-
 // The rows of one block as a contiguous range r0, r0 + 1, ...: the walk
 // steps one token at a time, so the shard index, the row inside the shard and
 // the shard's end position change by increments; the shard search runs only
