@@ -337,36 +337,31 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 
 // ------------------------------------------------------------- shard map --
 // The rows of one block as a contiguous range r0, r0 + 1, ...: the walk
-// steps one token at a time, so the shard index, the row inside the shard and
-// the shard's end position change by increments; the shard search runs only
-// when a step reaches the end of a shard or of a batch row.
+// steps one token at a time, so the row inside the shard moves by increments
+// and the shard lookup (a division and a search over the shard offsets) runs
+// only when a step leaves the current shard or batch row.
 struct RowWalk {
-  int64_t row, bi, si, local, end;
+  int64_t row;     // token index in the (b, s) grid
+  int64_t local;   // row index inside shard k's (b, s_k) tensor
+  int64_t left;    // rows until the current shard ends in this batch row
   int k;
 
   __device__ __forceinline__ void locate(const ShardMap& m) {
+    const int64_t bi = (m.b > 1 && m.s > 0) ? row / m.s : 0;
+    const int64_t si = row - bi * m.s;
+    k = 0;
     while (k + 1 < m.t && m.off[k + 1] <= si) ++k;   // skips empty shards
     local = bi * (m.off[k + 1] - m.off[k]) + (si - m.off[k]);
-    end = m.off[k + 1];
+    left = m.off[k + 1] - si;
   }
   __device__ __forceinline__ void init(const ShardMap& m, int64_t r) {
     row = r;
-    bi = (m.b > 1 && m.s > 0) ? r / m.s : 0;
-    si = r - bi * m.s;
-    k = 0;
     locate(m);
   }
   __device__ __forceinline__ void next(const ShardMap& m) {
     ++row;
     ++local;
-    if (++si == end) {
-      if (si == m.s) {
-        ++bi;
-        si = 0;
-        k = 0;
-      }
-      locate(m);
-    }
+    if (--left == 0) locate(m);
   }
 };
 
