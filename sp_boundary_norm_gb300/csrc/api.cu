@@ -278,18 +278,18 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
 const int kFwdStages[] = {3, 2};
 const int kBwdRing[] = {3, 2, 1};   // rows staged; 1 = no prefetch (very wide rows)
 
-// Forward threads per block: the largest of 256, 160, 128, 64 that splits the
-// row's h/8 vectors into at least 4 (else at least 2) full chunks, so no
-// thread idles in a last partial chunk and the per-row work is spread over
-// several chunks; blocks per SM are then 512 / threads (16 warps).
+// Forward threads per block: the first of 256, 128, 64 that splits the row's
+// h/8 vectors into at least 2 full chunks (no thread idles in a last partial
+// chunk, and the blocks fill an SM's 16 warps exactly), else 160 (three blocks
+// per SM); measured on GB300, fewer chunks of more threads beat more chunks of
+// fewer threads (h = 4096: 256 x 2 over 128 x 4 over 64 x 8).
 int fwd_threads(int64_t h) {
   const int64_t nvec = h / 8;
   const int forced = g_tune[0][2].load();
   if (forced != 0 && fwd_kernel(forced, 0, 2) != nullptr) return forced;
-  static const int opts[] = {256, 160, 128, 64};
-  for (int min_chunks : {4, 2})
-    for (int n : opts)
-      if (nvec % n == 0 && nvec / n >= min_chunks) return n;
+  static const int opts[] = {256, 128, 64, 160};
+  for (int n : opts)
+    if (nvec % n == 0 && nvec / n >= 2) return n;
   return nvec <= 64 ? 64 : 256;
 }
 
