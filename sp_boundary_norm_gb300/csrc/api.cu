@@ -521,8 +521,7 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   P.thr = static_cast<uint32_t>(std::floor(p * 4294967296.0));
   P.scale = static_cast<float>(1.0 / (1.0 - p));
   P.eps = eps;
-  P.key0 = static_cast<uint32_t>(seed);
-  P.key1 = static_cast<uint32_t>(seed >> 32);
+  philox_round_keys(seed, &P.rk);
   P.off0 = static_cast<uint32_t>(offset);
   P.off1 = static_cast<uint32_t>(offset >> 32);
   P.rows = rows;
@@ -602,8 +601,7 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
   P.thr = static_cast<uint32_t>(std::floor(p * 4294967296.0));
   P.scale = static_cast<float>(1.0 / (1.0 - p));
   P.eps = eps;
-  P.key0 = static_cast<uint32_t>(seed);
-  P.key1 = static_cast<uint32_t>(seed >> 32);
+  philox_round_keys(seed, &P.rk);
   P.off0 = static_cast<uint32_t>(offset);
   P.off1 = static_cast<uint32_t>(offset >> 32);
   P.rows = b * s;
@@ -793,8 +791,7 @@ static sp_status_t norm_bwd_common(
   P.scale = static_cast<float>(1.0 / (1.0 - p));
   // same keep rule as the forward: keep iff draw >= floor(p * 2^32)
   P.thr = static_cast<uint32_t>(std::floor(p * 4294967296.0));
-  P.key0 = static_cast<uint32_t>(seed);
-  P.key1 = static_cast<uint32_t>(seed >> 32);
+  philox_round_keys(seed, &P.rk);
   P.off0 = static_cast<uint32_t>(offset);
   P.off1 = static_cast<uint32_t>(offset >> 32);
   P.rows = rows;

@@ -166,11 +166,11 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
           const uint64_t q = static_cast<uint64_t>(grow + ch * kChunk) >> 2;
           const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
                                                    static_cast<uint32_t>(q >> 32), P.off0, P.off1),
-                                        P.key0, P.key1);
+                                        P.rk);
           const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
                                                    static_cast<uint32_t>((q + 1) >> 32), P.off0,
                                                    P.off1),
-                                        P.key0, P.key1);
+                                        P.rk);
           mk = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         } else {
           mk = lds8(it + off_mask - tid * 8);

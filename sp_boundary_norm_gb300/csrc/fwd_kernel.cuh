@@ -117,11 +117,11 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
           const uint64_t q = (e_row + cc) >> 2;
           const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
                                                    static_cast<uint32_t>(q >> 32), P.off0, P.off1),
-                                        P.key0, P.key1);
+                                        P.rk);
           const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
                                                    static_cast<uint32_t>((q + 1) >> 32), P.off0,
                                                    P.off1),
-                                        P.key0, P.key1);
+                                        P.rk);
           const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
           float ys[8];
 #pragma unroll

@@ -9,44 +9,33 @@
 namespace spb {
 
 // ----------------------------------------------------------------- Philox --
-// Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel Random
-// Numbers: As Easy as 1, 2, 3" (SC'11): per round, two 32x32->64-bit
-// multiplies of counter words 0 and 2 by fixed odd multipliers; the high
-// halves are xored with the other two counter words and the round key; the key
-// then advances by the Weyl increments (golden ratio, sqrt(3) - 1).
-constexpr uint32_t kPhiloxMul0 = 0xD2511F53u;
-constexpr uint32_t kPhiloxMul1 = 0xCD9E8D57u;
-constexpr uint32_t kPhiloxWeyl0 = 0x9E3779B9u;
-constexpr uint32_t kPhiloxWeyl1 = 0xBB67AE85u;
-
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32-10: per round, two 32x32->64-bit multiplies of counter words 0
+// and 2 by the fixed odd multipliers; the high halves are xored with the
+// other two counter words and the round key.  The round keys come from the
+// kernel parameters (one constant operand of each xor, no key arithmetic).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& rk) {
 #pragma unroll
   for (int round = 0; round < 10; ++round) {
     const uint64_t p0 = static_cast<uint64_t>(kPhiloxMul0) * c.x;
     const uint64_t p1 = static_cast<uint64_t>(kPhiloxMul1) * c.z;
     const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
     const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += kPhiloxWeyl0;
-    k1 += kPhiloxWeyl1;
+    c = make_uint4(hi1 ^ c.y ^ rk.k0[round], lo1, hi0 ^ c.w ^ rk.k1[round], lo0);
   }
   return c;
 }
 
-// Keep bits of the 8 consecutive elements starting at global element index
-// `e0` (a multiple of 8): element i keeps iff word (i & 3) of Philox at counter
-// (i >> 2, offset) is >= thr.  Bit e of the result is element e0 + e.
-__device__ __forceinline__ uint32_t keep_bits8(uint64_t e0, uint32_t thr, uint32_t k0,
-                                               uint32_t k1, uint32_t off0, uint32_t off1) {
-  const uint64_t q = e0 >> 2;
-  const uint4 a = philox4x32_10(
-      make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), off0, off1), k0, k1);
-  const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
-                                           static_cast<uint32_t>((q + 1) >> 32), off0, off1),
-                                k0, k1);
-  return (a.x >= thr ? 1u : 0u) | (a.y >= thr ? 2u : 0u) | (a.z >= thr ? 4u : 0u) |
-         (a.w >= thr ? 8u : 0u) | (b.x >= thr ? 16u : 0u) | (b.y >= thr ? 32u : 0u) |
-         (b.z >= thr ? 64u : 0u) | (b.w >= thr ? 128u : 0u);
+// The same from a bare key (k0, k1): the round keys are derived first.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  PhiloxKeys rk;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    rk.k0[round] = k0;
+    rk.k1[round] = k1;
+    k0 += kPhiloxWeyl0;
+    k1 += kPhiloxWeyl1;
+  }
+  return philox4x32_10(c, rk);
 }
 
 // ------------------------------------------------------------------- bf16 --
@@ -213,40 +202,8 @@ __device__ __forceinline__ uint32_t keep_bytes4(uint4 u, uint32_t thr) {
   return __byte_perm(__byte_perm(k0, k1, 0x3340), __byte_perm(k2, k3, 0x3340), 0x5410);
 }
 
-// Mask bytes (one 0/1 byte per element, element e in byte e) of the 8
-// consecutive elements starting at global element index e0 (a multiple of 8).
-__device__ __forceinline__ uint2 keep_mask8(uint64_t e0, uint32_t thr, uint32_t k0, uint32_t k1,
-                                            uint32_t off0, uint32_t off1) {
-  const uint64_t q = e0 >> 2;
-  const uint4 a = philox4x32_10(
-      make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), off0, off1), k0, k1);
-  const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
-                                           static_cast<uint32_t>((q + 1) >> 32), off0, off1),
-                                k0, k1);
-  return make_uint2(keep_bytes4(a, thr), keep_bytes4(b, thr));
-}
 
-// 8 mask bytes (0/1) from 8 keep bits.
-__device__ __forceinline__ uint2 bits_to_bytes8(uint32_t bits) {
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    lo |= ((bits >> e) & 1u) << (8 * e);
-    hi |= ((bits >> (e + 4)) & 1u) << (8 * e);
-  }
-  return make_uint2(lo, hi);
-}
 
-// 8 keep bits from 8 mask bytes (any nonzero byte = kept).
-__device__ __forceinline__ uint32_t bytes8_to_bits(uint2 m) {
-  uint32_t bits = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    bits |= (((m.x >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << e;
-    bits |= (((m.y >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << (e + 4);
-  }
-  return bits;
-}
 
 // ----------------------------------------------------- memory primitives --
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

@@ -8,6 +8,31 @@
 
 namespace spb {
 
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As
+// Easy as 1, 2, 3", SC'11): the two round multipliers and the Weyl key
+// increments (golden ratio, sqrt(3) - 1).
+constexpr uint32_t kPhiloxMul0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxMul1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxWeyl0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxWeyl1 = 0xBB67AE85u;
+
+// The key of each of the ten rounds, (k0 + r * W0, k1 + r * W1) mod 2^32 for
+// round r: fixed per seed, so it is computed once on the host and read by the
+// kernels from their parameters.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+inline void philox_round_keys(uint64_t seed, PhiloxKeys* rk) {
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    rk->k0[r] = k0;
+    rk->k1[r] = k1;
+    k0 += kPhiloxWeyl0;
+    k1 += kPhiloxWeyl1;
+  }
+}
+
 // Where each token of the (b, s) token grid lives: sequence shard k holds
 // positions [off[k], off[k+1]) of every batch row (o_k = floor(k*s/t)).
 struct ShardMap {
@@ -35,7 +60,7 @@ struct FwdParams {
   uint32_t thr;          // keep iff draw >= thr; 0 disables dropout
   float scale;           // float(1/(1-p))
   float eps;
-  uint32_t key0, key1;   // Philox key = seed
+  PhiloxKeys rk;         // Philox round keys of the seed
   uint32_t off0, off1;   // Philox counter words 2, 3 = offset
   int64_t rows;          // b * s
   int32_t* status;
@@ -59,7 +84,7 @@ struct BwdParams {
   int32_t has_skip;
   float scale;
   uint32_t thr;          // mask regeneration (mask-free backward): keep iff draw >= thr
-  uint32_t key0, key1;   // Philox key = the forward's seed
+  PhiloxKeys rk;         // Philox round keys of the forward's seed
   uint32_t off0, off1;   // Philox counter offset = the forward's offset
   int64_t rows;
   float* ws;             // [gridDim.x][3][h] per-block parameter-gradient partials
