@@ -325,7 +325,7 @@ LaunchShape fwd_shape_uncached(int64_t rows, int64_t h, int t) {
   const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
-  const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float);
+  const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float2);
   return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 2,
                     /*stages=*/3, /*blocks per SM=*/512 / threads,
                     [&](int st) { return fwd_kernel(threads, t, st); });
@@ -336,7 +336,7 @@ LaunchShape fwd_shard_shape_uncached(int64_t rows, int64_t h) {
   const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(2) * threads * 16;
-  const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float);
+  const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float2);
   return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 2,
                     /*stages=*/3, /*blocks per SM=*/512 / threads,
                     [&](int st) { return fwd_shard_kernel(threads, st); });

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
   constexpr int kStream = NTHR * 16;
   const int stage_bytes = (t + 1) * kStream;
   uint8_t* zbuf = smem + STAGES * stage_bytes + tid * 16;   // own slots, stride kStream
-  float* red = reinterpret_cast<float*>(smem + STAGES * stage_bytes + nchunk * kStream);
+  float2* red = reinterpret_cast<float2*>(smem + STAGES * stage_bytes + nchunk * kStream);   // [2][32]
   const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
     const uint64_t e_row = static_cast<uint64_t>(row * h + c0);   // global element index
 
     // ---- pass 1: g* sum, bias, dropout, residual -> Z (stored) ----------
-    float lsum = 0.f;
+    float lsum = 0.f, lsq = 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < nchunk; ++ch) {
       issue_next();
@@ -136,45 +136,59 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
         st16_stream(zrow + cc, zb);
         st8_stream(mrow + cc, keep);
         *reinterpret_cast<uint4*>(zbuf + ch * kStream) = zb;
-        // the norm sees the stored bf16 values
-        float l2[2] = {0.f, 0.f};
+        // the norm sees the stored bf16 values: sum of Z (LayerNorm) and sum
+        // of Z^2 (both norms)
+        float q2[2] = {0.f, 0.f};
+        fma2_bf16(zb.x, zb.x, q2[0], q2[1]);
+        fma2_bf16(zb.y, zb.y, q2[0], q2[1]);
+        fma2_bf16(zb.z, zb.z, q2[0], q2[1]);
+        fma2_bf16(zb.w, zb.w, q2[0], q2[1]);
+        lsq += q2[0] + q2[1];
         if (is_ln) {
+          float l2[2] = {0.f, 0.f};
           add2_bf16(zb.x, l2[0], l2[1]);
           add2_bf16(zb.y, l2[0], l2[1]);
           add2_bf16(zb.z, l2[0], l2[1]);
           add2_bf16(zb.w, l2[0], l2[1]);
-        } else {
-          fma2_bf16(zb.x, zb.x, l2[0], l2[1]);
-          fma2_bf16(zb.y, zb.y, l2[0], l2[1]);
-          fma2_bf16(zb.z, zb.z, l2[0], l2[1]);
-          fma2_bf16(zb.w, zb.w, l2[0], l2[1]);
+          lsum += l2[0] + l2[1];
         }
-        lsum += l2[0] + l2[1];
       }
       stage = (stage + 1 == STAGES) ? 0 : stage + 1;
     }
 
     // ---- token-wise statistics over h ------------------------------------
+    // LayerNorm: the two sums are reduced together (one block barrier) and
+    // the biased variance is taken as E[Z^2] - mean^2 when mean^2 <= var / 4:
+    // there the float32 cancellation error stays within a few 1e-6 of var
+    // (the terms are at most 1.25 var).  Otherwise (a row whose mean is large
+    // against its spread, or a non-finite value) the variance is recomputed
+    // in a second pass as the mean of (Z - mean)^2.
     float mean = 0.f, rstd;
     if (is_ln) {
-      mean = block_sum(lsum, red + 32 * slot_sel) * inv_h;
+      const float2 sums = block_sum2(lsum, lsq, red + 32 * slot_sel);
       slot_sel ^= 1;
-      float lsqa = 0.f, lsqb = 0.f;
-      const float nmean = -mean;
+      mean = sums.x * inv_h;
+      const float var1 = sums.y * inv_h - mean * mean;
+      if (mean * mean <= 0.25f * var1) {
+        rstd = rsqrtf(var1 + P.eps);
+      } else {
+        float lsqa = 0.f, lsqb = 0.f;
+        const float nmean = -mean;
 #pragma unroll 1
-      for (int ch = 0; ch < nchunk; ++ch) {
-        if (ch * kChunk + c0 < h) {
-          float d[8];
-          add8_bf16_bcast(lds16(zbuf + ch * kStream), nmean, d);   // z - mean
+        for (int ch = 0; ch < nchunk; ++ch) {
+          if (ch * kChunk + c0 < h) {
+            float d[8];
+            add8_bf16_bcast(lds16(zbuf + ch * kStream), nmean, d);   // z - mean
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
+            for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
+          }
         }
+        const float var = block_sum(lsqa + lsqb, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
+        slot_sel ^= 1;
+        rstd = rsqrtf(var + P.eps);
       }
-      const float var = block_sum(lsqa + lsqb, red + 32 * slot_sel) * inv_h;
-      slot_sel ^= 1;
-      rstd = rsqrtf(var + P.eps);
     } else {
-      const float ms = block_sum(lsum, red + 32 * slot_sel) * inv_h;
+      const float ms = block_sum(lsq, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
       slot_sel ^= 1;
       rstd = rsqrtf(ms + P.eps);
     }

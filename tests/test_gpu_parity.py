@@ -56,6 +56,28 @@ def test_forward_full_compare(name):
     _full_fwd_compare(w, inp, out)
 
 
+def test_layernorm_rows_with_large_mean():
+    """The forward takes the LayerNorm variance as E[Z^2] - mean^2 only where
+    mean^2 <= var / 4 and recomputes it from (Z - mean)^2 elsewhere.  Residual
+    rows shifted by 0 to 300 standard deviations (either sign, several near the
+    switch at 0.5) put tokens on both sides; all must meet the tolerances."""
+    w = wl.Workload("lm", t=4, b=1, s=288, h=1024, draw_seed=97)
+    inp = wl.forward_inputs(w, C.DEV)
+    shifts = [0.0, 0.25, 0.45, 0.49, 0.5, 0.51, 0.55, 0.7, 1.0, 3.0, 30.0, 300.0, -0.5, -40.0]
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    for k, r in enumerate(inp["residual"]):
+        g = torch.arange(offs[k], offs[k + 1], device=C.DEV)
+        c = torch.tensor(shifts, device=C.DEV)[g % len(shifts)]
+        inp["residual"][k] = (r.float() + c[None, :, None]).to(torch.bfloat16)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    ref = _full_fwd_compare(w, inp, out)
+    ratio = np.concatenate([m * m / (1.0 / (r * r) - w.eps) for m, r in
+                            zip(ref["mean"], ref["rstd"])], axis=1)
+    assert (ratio < 0.2).any() and (ratio > 0.3).any() and (ratio > 1e3).any()
+
+
 @pytest.mark.parametrize("variant", [
     dict(norm="rmsnorm", eps=1e-6),
     dict(p=0.0),
