@@ -231,9 +231,11 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z,
  * own device memory (SP_NOALLOC_WORKSPACE_BYTES on every GPU that loads the
  * library, held until the process exits).  Nothing is allocated or freed by
  * the call.
- *  - Shapes whose workspace (sp_norm_bwd_workspace_bytes) exceeds
+ *  - Shapes whose partials (one float32 row of 3*h per block of this call's
+ *    own launch: the stored-mask backward, with or without dz_skip) exceed
  *    SP_NOALLOC_WORKSPACE_BYTES are rejected with SP_ERR_UNSUPPORTED before
- *    anything is enqueued.
+ *    anything is enqueued.  h = 8192 (152 blocks on a 152-SM GPU) fits;
+ *    h = 5120 (304 blocks) and h = 16384 do not.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture
  *    on that device.

@@ -293,10 +293,15 @@ int fwd_threads(int64_t h) {
   return nvec <= 64 ? 64 : 256;
 }
 
-// Backward (threads, chunks per row): two full chunks per thread where a
-// shape fits exactly (the per-thread parameter-gradient registers grow with
-// the chunks), else one, else the smallest shape that covers the row.
-void bwd_threads(int64_t h, int* threads, int* maxc) {
+// Backward (threads, chunks per row): a shape that covers the row exactly,
+// in this order of preference (measured on GB300): two chunks per thread with
+// the parameter-gradient terms in registers (512, 256, 128 threads); for the
+// mask-free variant at h = 8192, four chunks of 256 threads with the terms in
+// tensor memory (its Philox draws need the registers); two chunks of 320
+// threads with the terms in tensor memory (h = 5120: 20 warps per SM instead
+// of one 640-thread block); one chunk (640, 512, 256, 64 threads).  Other h:
+// the smallest register shape that covers the row.
+void bwd_threads(int64_t h, bool regen, int* threads, int* maxc) {
   const int64_t nvec = h / 8;
   const int ft = g_tune[1][2].load(), fc = g_tune[1][3].load();
   if (ft != 0 && fc != 0 && static_cast<int64_t>(ft) * fc * 8 >= h &&
@@ -305,7 +310,12 @@ void bwd_threads(int64_t h, int* threads, int* maxc) {
     *maxc = fc;
     return;
   }
-  static const int opts[][2] = {{512, 2}, {256, 2}, {128, 2}, {640, 1},
+  if (regen && nvec == 1024) {
+    *threads = 256;
+    *maxc = 4;
+    return;
+  }
+  static const int opts[][2] = {{512, 2}, {256, 2}, {128, 2}, {320, 2}, {640, 1},
                                 {512, 1}, {256, 1}, {64, 1}};
   for (const auto& o : opts) {
     if (nvec == static_cast<int64_t>(o[0]) * o[1]) {
@@ -374,15 +384,28 @@ LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip)
 
 LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool regen) {
   int threads, maxc;
-  bwd_threads(h, &threads, &maxc);
+  bwd_threads(h, regen, &threads, &maxc);
   const size_t item =
       static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
   const size_t ring_row = item * maxc;
-  return pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing, 3,
-                    /*ring=*/2, /*blocks per SM=*/threads <= 256 ? 512 / threads : 1, [&](int st) {
-                      return regen ? bwd_regen_kernel(threads, maxc, st)
-                                   : bwd_kernel(threads, maxc, st);
-                    });
+  const bool tacc = bwd_tmem_shape(threads, maxc);
+  const int cap = tacc ? 512 / bwd_tmem_cols(threads, maxc) : (threads <= 256 ? 512 / threads : 1);
+  LaunchShape ls = pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing,
+                              3, /*ring=*/2, /*blocks per SM=*/cap, [&](int st) {
+                                return regen ? bwd_regen_kernel(threads, maxc, st)
+                                             : bwd_kernel(threads, maxc, st);
+                              });
+  if (tacc && ls.fits) {
+    // The blocks of an SM share its 512 tensor-memory columns: pad the shared
+    // memory so that no more than `cap` blocks can be resident on one SM (an
+    // allocation beyond the columns would wait for a block to finish).
+    const size_t floor = kSmemPerSm / (cap + 1) - kReserve + 16;
+    if (ls.smem < floor) ls.smem = floor;
+    ls.fits = ls.smem <= kSmemPerBlock;
+    const int64_t most = static_cast<int64_t>(device_sm_count()) * cap;
+    ls.grid = static_cast<int>(rows < most ? (rows > 0 ? rows : 1) : most);
+  }
+  return ls;
 }
 
 LaunchShape fwd_shape(int64_t rows, int64_t h, int t) {
@@ -418,6 +441,11 @@ cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStre
 
 sp_status_t record_error(sp_status_t code, const char* message) {
   return fail(code, "%s", message);
+}
+
+size_t stored_mask_bwd_workspace_bytes(int64_t rows, int64_t h, bool has_skip) {
+  const LaunchShape ls = bwd_shape(rows, h, has_skip, false);
+  return static_cast<size_t>(ls.grid) * 3 * static_cast<size_t>(h) * sizeof(float);
 }
 
 int device_sm_count() {

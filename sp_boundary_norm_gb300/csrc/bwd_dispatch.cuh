@@ -16,7 +16,9 @@ static const void* bwd_kernel_s(int ring) {
 }
 
 // Instantiated shapes (threads, chunks per row): (64, 1), (128, 2), (256, 1),
-// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1); ring of 1, 2 or 3 rows.
+// (256, 2), (512, 1), (512, 2), (512, 4), (640, 1) with the parameter-gradient
+// terms in registers, (128, 4), (256, 4), (320, 2) with them in tensor memory;
+// ring of 1, 2 or 3 rows.
 template <bool REGEN>
 static const void* bwd_kernel_any(int threads, int maxc, int ring) {
   switch (threads * 8 + maxc) {
@@ -24,6 +26,9 @@ static const void* bwd_kernel_any(int threads, int maxc, int ring) {
     case 128 * 8 + 2: return bwd_kernel_s<128, 2, REGEN>(ring);
     case 256 * 8 + 1: return bwd_kernel_s<256, 1, REGEN>(ring);
     case 256 * 8 + 2: return bwd_kernel_s<256, 2, REGEN>(ring);
+    case 128 * 8 + 4: return bwd_kernel_s<128, 4, REGEN>(ring);
+    case 256 * 8 + 4: return bwd_kernel_s<256, 4, REGEN>(ring);
+    case 320 * 8 + 2: return bwd_kernel_s<320, 2, REGEN>(ring);
     case 512 * 8 + 1: return bwd_kernel_s<512, 1, REGEN>(ring);
     case 512 * 8 + 2: return bwd_kernel_s<512, 2, REGEN>(ring);
     case 512 * 8 + 4: return bwd_kernel_s<512, 4, REGEN>(ring);

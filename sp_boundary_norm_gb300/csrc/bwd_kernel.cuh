@@ -9,11 +9,35 @@ namespace spb {
 // REGEN = true: the mask-free variant; the dropout keep decisions are drawn
 // again from Philox4x32-10 at the element's global index (the forward's seed
 // and offset) instead of being read from the stored 1-byte mask.
+// Shapes with bwd_tmem_shape(NTHR, MAXC) keep each thread's dgamma / dbeta /
+// dbias terms in tensor memory (its lane, 24 columns per chunk), which frees
+// the registers for wider rows per thread at 16 warps per SM; the others keep
+// them in registers.
 template <int NTHR, int MAXC, int RING, bool REGEN>
-__global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
+__global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
+                                            ? 512 / bwd_tmem_cols(NTHR, MAXC)
+                                            : (NTHR <= 256 ? 512 / NTHR : 1))
     norm_bwd_kernel(const BwdParams P) {
+  constexpr bool TACC = bwd_tmem_shape(NTHR, MAXC);
+  constexpr uint32_t kCols = bwd_tmem_cols(NTHR, MAXC);
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x;
+  // tensor memory: allocated by warp 0 before anything can diverge
+  uint32_t tacc = 0;   // this thread's lane, first of its columns
+  if constexpr (TACC) {
+    if (tid < 32) tmem_alloc(&tmem_base, kCols);
+    tmem_sync_block();
+    const int w = tid >> 5;
+    tacc = tmem_base + (static_cast<uint32_t>(32 * (w & 3)) << 16) +
+           static_cast<uint32_t>((w >> 2) * 24 * MAXC);
+    const float zero[16] = {};
+#pragma unroll
+    for (int ch = 0; ch < MAXC; ++ch) {
+      tmem_st16(tacc + 24 * ch, zero);
+      tmem_st8(tacc + 24 * ch + 16, zero);
+    }
+  }
   const int h = static_cast<int>(P.map.h);   // <= SP_MAX_HIDDEN
   constexpr int kChunk = 8 * NTHR;
   const int nchunk = (h + kChunk - 1) / kChunk;
@@ -124,8 +148,16 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
     // exact product of two bf16 values
     const float nmean = is_ln ? -mean : 0.f;
     float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
+    if constexpr (TACC) tmem_wait_st();   // the previous row's stores have landed
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
+      float gb[16];   // this chunk's dgamma terms, then its dbeta terms
+      if constexpr (TACC) {
+        tmem_ld16(tacc + 24 * ch, gb);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gb[e] = acc_g[ch][e], gb[8 + e] = acc_b[ch][e];
+      }
       if ((valid >> ch) & 1u) {
         const uint8_t* it = it0 + ch * item_bytes;
         const uint4 dyv = lds16(it);
@@ -133,15 +165,21 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
         float xh[8], dxh[8], dy[8];
         add8_bf16_bcast(zv, nmean, xh);             // z - mean
         fma8_bf16_bcast(dyv, gam[ch], 0.f, dxh);    // dY * gamma
-        if (is_ln) add8_bf16(dyv, acc_b[ch]);       // dbeta terms
+        if (is_ln) add8_bf16(dyv, gb + 8);          // dbeta terms
         unpack8(dyv, dy);
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
           mul2(xh[e], xh[e + 1], rstd, rstd);
           add2(s1a, s1b, dxh[e], dxh[e + 1]);
           fma2(s2a, s2b, dxh[e], dxh[e + 1], xh[e], xh[e + 1]);
-          fma2(acc_g[ch][e], acc_g[ch][e + 1], dy[e], dy[e + 1], xh[e], xh[e + 1]);
+          fma2(gb[e], gb[e + 1], dy[e], dy[e + 1], xh[e], xh[e + 1]);
         }
+      }
+      if constexpr (TACC) {
+        tmem_st16(tacc + 24 * ch, gb);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc_g[ch][e] = gb[e], acc_b[ch][e] = gb[8 + e];
       }
     }
 
@@ -157,6 +195,13 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
     uint16_t* dg0_row = P.n_gather > 0 ? P.dgathered[0] + grow : nullptr;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
+      float bt[8];   // this chunk's dbias terms
+      if constexpr (TACC) {
+        tmem_ld8(tacc + 24 * ch + 16, bt);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bt[e] = acc_bias[ch][e];
+      }
       if ((valid >> ch) & 1u) {
         const uint8_t* it = it0 + ch * item_bytes;
         const uint4 dyv = lds16(it);
@@ -193,15 +238,38 @@ __global__ void __launch_bounds__(NTHR, (NTHR <= 256 ? 512 / NTHR : 1))
           dp[e] = kept ? dp[e] : 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) add2(acc_bias[ch][e], acc_bias[ch][e + 1], dp[e], dp[e + 1]);
+        for (int e = 0; e < 8; e += 2) add2(bt[e], bt[e + 1], dp[e], dp[e + 1]);
         st16_stream(dres_row + ch * kChunk, pack8(dz));
         const uint4 pb = pack8(dp);
         if (dg0_row != nullptr) st16_stream(dg0_row + ch * kChunk, pb);
         for (int j = 1; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
       }
+      if constexpr (TACC) {
+        tmem_st8(tacc + 24 * ch + 16, bt);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc_bias[ch][e] = bt[e];
+      }
     }
   }
   cp_async_wait<0>();
+  if constexpr (TACC) {
+    tmem_wait_st();
+#pragma unroll
+    for (int ch = 0; ch < MAXC; ++ch) {
+      float gb[16], bt[8];
+      tmem_ld16(tacc + 24 * ch, gb);
+      tmem_ld8(tacc + 24 * ch + 16, bt);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc_g[ch][e] = gb[e];
+        acc_b[ch][e] = gb[8 + e];
+        acc_bias[ch][e] = bt[e];
+      }
+    }
+    tmem_sync_block();   // every warp is done with tensor memory
+    if (tid < 32) tmem_dealloc(tmem_base, kCols);
+  }
 
   // per-block partials: ws[block][0|1|2][c] = dgamma | dbeta | dbias terms
   float* wsb = P.ws + static_cast<int64_t>(blockIdx.x) * 3 * h;

@@ -57,7 +57,9 @@ extern "C" sp_status_t sp_norm_bwd_noalloc(
     const int32_t* cu_seqlens, int32_t n_seqs, sp_norm_t norm, void* const* dresidual,
     void* const* dgathered, int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
     int32_t* dev_status, void* stream) {
-  const size_t need = sp_norm_bwd_workspace_bytes(b, s, h, t, norm);
+  const bool valid_shape = b > 0 && s > 0 && h >= 8 && h % 8 == 0 && h <= SP_MAX_HIDDEN;
+  const size_t need = valid_shape ? spb::stored_mask_bwd_workspace_bytes(b * s, h, dz_skip != nullptr)
+                                  : 0;
   if (need > SP_NOALLOC_WORKSPACE_BYTES) {
     return spb::record_error(
         SP_ERR_UNSUPPORTED,

@@ -19,6 +19,20 @@ constexpr uint32_t kPhiloxWeyl1 = 0xBB67AE85u;
 // The key of each of the ten rounds, (k0 + r * W0, k1 + r * W1) mod 2^32 for
 // round r: fixed per seed, so it is computed once on the host and read by the
 // kernels from their parameters.
+// Backward launch shapes (threads, chunks per row) whose per-thread
+// parameter-gradient terms live in tensor memory instead of registers, and
+// the tensor-memory columns one block of them allocates: 24 columns per chunk
+// (dgamma, dbeta, dbias terms of 8 channels) for each warp sharing a lane
+// quarter, rounded up to a power of two.  512 / columns blocks fit an SM.
+__host__ __device__ constexpr bool bwd_tmem_shape(int nthr, int maxc) {
+  return (nthr == 256 && maxc == 4) || (nthr == 128 && maxc == 4) || (nthr == 320 && maxc == 2);
+}
+__host__ __device__ constexpr int bwd_tmem_cols(int nthr, int maxc) {
+  int need = ((nthr / 32 + 3) / 4) * 24 * maxc, c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
+
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
@@ -135,6 +149,10 @@ const void* bwd_regen_kernel(int threads, int maxc, int ring);
 // (threads, chunks per row, ranks t, chunk stages).
 const void* rs_bwd_kernel(int threads, int maxc, int t, int stages);
 
+// Workspace bytes of one sp_norm_bwd call (stored mask) of `rows` tokens of
+// width h (0 for shapes outside the limits): its own launch grid, not the
+// maximum over the backward variants that sp_norm_bwd_workspace_bytes reports.
+size_t stored_mask_bwd_workspace_bytes(int64_t rows, int64_t h, bool has_skip);
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st);
 cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st);
 cudaError_t launch_reduce_scatter(const CopyParams& p, int t, cudaStream_t st);

@@ -436,6 +436,61 @@ def test_unfused_mask_equals_fused_mask():
         assert torch.equal(a, b)
 
 
+# ------------------------------------- tensor-memory parameter-gradient terms
+
+@pytest.fixture
+def bwd_shape():
+    """Force the backward's launch shape (threads, chunks per row, ring rows)
+    for one test; the automatic choice is restored afterwards."""
+    def force(threads, chunks, ring=2):
+        C.sp.sp_debug_tune(1, ring, 0, threads, chunks)
+    yield force
+    C.sp.sp_debug_tune(1, 0, 0, 0, 0)
+
+
+@pytest.mark.parametrize("shape,h", [((256, 4), 8192), ((256, 4), 6152), ((128, 4), 4096),
+                                     ((128, 4), 3000), ((320, 2), 5120), ((320, 2), 4000)])
+def test_backward_tensor_memory_shapes(bwd_shape, shape, h):
+    """The shapes that keep each thread's dgamma / dbeta / dbias terms in
+    tensor memory: exact rows and a ragged last chunk, several rows per block."""
+    bwd_shape(*shape)
+    w = wl.Workload("tm", t=2, b=1, s=1216, h=h, draw_seed=101)
+    inp, fwd, b, out = _bwd_setup(w)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], None, out, C.sample_tokens(w, 96))
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
+
+
+@pytest.mark.parametrize("variant", [dict(ring=1), dict(ring=3), dict(norm="rmsnorm", eps=1e-6),
+                                     dict(skip=True), dict(n_gather=2), dict(t=3, s=96)])
+def test_backward_tensor_memory_variants(bwd_shape, variant):
+    v = dict(variant)
+    bwd_shape(256, 4, v.pop("ring", 2))
+    skip = v.pop("skip", False)
+    w = wl.Workload("tv", t=2, b=1, s=640, h=8192, draw_seed=102).with_(**v)
+    inp, fwd, b, out = _bwd_setup(w, skip, n_gather=w.n_gather)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out, C.sample_tokens(w, 64))
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out)
+
+
+def test_backward_tensor_memory_mask_free_and_deterministic(bwd_shape):
+    bwd_shape(256, 4)
+    w = wl.Workload("td", t=2, b=1, s=640, h=8192, draw_seed=103)
+    inp, fwd, b, first = _bwd_setup(w)
+    again = C.run_bwd(w, fwd, inp["gamma"], b["dy"], None, n_gather=1)
+    got = C.alloc_bwd(w, 1)
+    C.sp.sp_norm_bwd_philox(b["dy"], fwd["z"], fwd["mean"], fwd["rstd"], inp["gamma"], None,
+                            s=w.s, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                            dresidual=got["dres"], dgathered=got["dgat"], dgamma=got["dgamma"],
+                            dbeta=got["dbeta"], dbias=got["dbias"], workspace=got["ws"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    for other in (again, got):
+        for a, c in zip(first["dres"] + first["dgat"], other["dres"] + other["dgat"]):
+            assert torch.equal(a, c)
+        for name in ("dgamma", "dbeta", "dbias"):
+            assert torch.equal(first[name], other[name]), name
+
+
 # ------------------------------------------------------ mask-free backward
 
 @pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(t=3, s=48),
