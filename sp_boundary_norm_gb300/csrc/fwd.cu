@@ -9,9 +9,11 @@
 // normalised row straight into the all-gather destination(s).
 //
 // Work layout: a persistent grid (16 warps per SM); block b of G processes
-// a contiguous range of about rows/G tokens, walked one token at a time (the
-// shard and the row inside the shard move by increments, so no per-row
-// division or shard search).  A row of h channels is cut into chunks of 8*T
+// tokens b, b + G, b + 2G, ... when every block gets at least 32 rows (the
+// blocks then stream neighbouring rows together: 0.7 % faster on the 70B
+// shape), else a contiguous range of about rows/G tokens; either way the walk
+// moves the shard and the row inside it by increments (no per-row division or
+// shard search).  A row of h channels is cut into chunks of 8*T
 // channels (T = threads); in each chunk thread i owns channels [8i, 8i+8).
 // Every thread streams its own 16-byte pieces of the t + 1 input rows into
 // its own shared-memory slots with cp.async, STAGES - 1 chunks ahead, so the

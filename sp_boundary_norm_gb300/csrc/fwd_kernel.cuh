@@ -33,8 +33,19 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
   // this block's rows: a contiguous range
+  // this block's rows: every G-th token from blockIdx.x when blocks get many
+  // rows (neighbouring tokens are then in flight together), else a
+  // contiguous range
+  const int64_t G = gridDim.x;
+  const bool strided = P.rows >= 32 * G;
+  const int64_t step = strided ? G : 1;
   int64_t r0, nrows;
-  block_rows(P.rows, blockIdx.x, gridDim.x, &r0, &nrows);
+  if (strided) {
+    r0 = blockIdx.x;
+    nrows = (P.rows - 1 - r0) / G + 1;
+  } else {
+    block_rows(P.rows, blockIdx.x, G, &r0, &nrows);
+  }
   const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
 
   // ---- prefetch cursor: the next (row, chunk) item to stage -------------
@@ -61,7 +72,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
       if (++pf_chunk == nchunk) {
         pf_chunk = 0;
         if (++pf_ri < nrows) {
-          pf.next(P.map);
+          pf.next(P.map, step);
           pf_goff = pf.row * h + c0;
           pf_roff = pf.local * h + c0;
         }
@@ -83,7 +94,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
   int slot_sel = 0;
   const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
-    if (ri > 0) cur.next(P.map);
+    if (ri > 0) cur.next(P.map, step);
     const int64_t row = cur.row;
     const int k = cur.k;
     const int64_t local = cur.local;

@@ -381,10 +381,11 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 }
 
 // ------------------------------------------------------------- shard map --
-// The rows of one block as a contiguous range r0, r0 + 1, ...: the walk
-// steps one token at a time, so the row inside the shard moves by increments
-// and the shard lookup (a division and a search over the shard offsets) runs
-// only when a step leaves the current shard or batch row.
+// The rows of one block, walked as r0, r0 + step, r0 + 2 step, ... (step 1:
+// a contiguous range; step = grid: every grid-th token): the row inside the
+// shard moves by increments, and the shard lookup (a division and a search
+// over the shard offsets) runs only when a step leaves the current shard or
+// batch row.
 struct RowWalk {
   int64_t row;     // token index in the (b, s) grid
   int64_t local;   // row index inside shard k's (b, s_k) tensor
@@ -407,6 +408,12 @@ struct RowWalk {
     ++row;
     ++local;
     if (--left == 0) locate(m);
+  }
+  __device__ __forceinline__ void next(const ShardMap& m, int64_t step) {
+    row += step;
+    local += step;
+    left -= step;
+    if (left <= 0) locate(m);
   }
 };
 
