@@ -436,6 +436,42 @@ def test_unfused_mask_equals_fused_mask():
         assert torch.equal(a, b)
 
 
+def test_graph_replay_of_a_step_equals_eager_calls():
+    """A step (forward, then the backward that reads its Z, mask and stats,
+    then the parameter reduce) captured in one CUDA graph, as bench.py times
+    it, and replayed twice gives the eager results bit for bit."""
+    w = wl.Workload("gr", t=4, b=1, s=2048, h=4096, draw_seed=111)
+    inp = wl.forward_inputs(w, C.DEV)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    fwd_e = C.run_fwd(w, inp)
+    bwd_e = C.run_bwd(w, fwd_e, inp["gamma"], dy, None, n_gather=1)
+    torch.cuda.synchronize()
+    fwd_g, bwd_g = C.alloc_fwd(w, 1, fill=7.0), C.alloc_bwd(w, 1)
+    for t in fwd_g["z"] + fwd_g["gathered"] + bwd_g["dres"] + bwd_g["dgat"]:
+        t.fill_(7.0)
+    C.run_fwd(w, inp, out=fwd_g)                      # warm-up outside the capture
+    C.run_bwd(w, fwd_g, inp["gamma"], dy, None, n_gather=1, out=bwd_g)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        C.run_fwd(w, inp, out=fwd_g)
+        C.run_bwd(w, fwd_g, inp["gamma"], dy, None, n_gather=1, out=bwd_g)
+    for _ in range(2):
+        for t in fwd_g["z"] + fwd_g["gathered"] + bwd_g["dres"] + bwd_g["dgat"]:
+            t.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        C.sp.check_device_status(C.DEV)
+        for key in ("z", "mask", "mean", "rstd", "gathered"):
+            for a, b in zip(fwd_e[key], fwd_g[key]):
+                assert torch.equal(a, b), key
+        for key in ("dres", "dgat"):
+            for a, b in zip(bwd_e[key], bwd_g[key]):
+                assert torch.equal(a, b), key
+        for key in ("dgamma", "dbeta", "dbias"):
+            assert torch.equal(bwd_e[key], bwd_g[key]), key
+
+
 # ------------------------------------- tensor-memory parameter-gradient terms
 
 @pytest.fixture
