@@ -50,7 +50,8 @@ typedef enum sp_status {
   SP_OK = 0,
   SP_ERR_INVALID_ARG = 1,   /* a size, count, probability or pointer is invalid */
   SP_ERR_MISALIGNED = 2,    /* a tensor pointer is not 16-byte aligned */
-  SP_ERR_UNSUPPORTED = 3,   /* valid request outside this build (e.g. h > SP_MAX_HIDDEN) */
+  SP_ERR_UNSUPPORTED = 3,   /* valid request outside this build (h > SP_MAX_HIDDEN, or no
+                               launch shape of the kernel fits one SM's shared memory) */
   SP_ERR_CUDA = 4,          /* a CUDA runtime error (text in sp_last_error) */
   SP_ERR_TIMEOUT = 5,       /* a bounded device-side wait expired (via dev_status) */
   SP_ERR_DEVICE_CHECK = 6,  /* device-side validation failed (via dev_status) */
