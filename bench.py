@@ -36,6 +36,7 @@ UNIT = "tokens/s"
 FWD_SOURCES = ("sp_boundary_norm_gb300/csrc/fwd.cu", "sp_boundary_norm_gb300/csrc/fwd_kernel.cuh",
                "sp_boundary_norm_gb300/csrc/sp_device.cuh", "sp_boundary_norm_gb300/csrc/sp_internal.h")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "rs_norm_fwd_kernel_70b.md")
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e nominal bandwidth (context; the roofline uses the measured copy)
 
 
 # ------------------------------------------------------------ byte counts --
@@ -582,6 +583,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world} (independent batches)"},
         "hbm_gbs": round((fb + bb) / (step_ms / 1e3) / 1e9, 1),
         "hbm_frac_of_peak": round((fb + bb) / (step_ms / 1e3) / 1e9 / peak, 4),
+        "hbm_frac_of_nominal": round((fb + bb) / (step_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
         "fwd": {"ms": round(fwd_avg, 4), "gbs": round(achieved, 1),
                 "bytes": fb, "tokens_per_s": round(w.tokens / (fwd_avg / 1e3), 1)},
         "bwd": {"ms": round(bwd_avg, 4), "gbs": round(bb / (bwd_avg / 1e3) / 1e9, 1),
