@@ -44,7 +44,12 @@ __global__ void __launch_bounds__(kCopyThreads) allgather_kernel(const CopyParam
   }
 }
 
-// shards[k][local] = bf16(sum over r ascending of partials[r][row]), float32.
+// shards[k][local] = bf16(sum over r ascending of partials[r][row]), float32
+// (each add widens its bf16 operand exactly: ((P_0 + P_1) + P_2) + ...).  A
+// thread issues the loads of all the partials of its 8 channels before it
+// adds them (TT = t known at compile time), or groups of four (TT = 0), so
+// several loads are in flight per thread.
+template <int TT>
 __global__ void __launch_bounds__(kCopyThreads) reduce_scatter_kernel(const CopyParams P,
                                                                       int t) {
   if (blockIdx.x == 0 && threadIdx.x < 32)
@@ -61,12 +66,25 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_scatter_kernel(const Copy
     uint16_t* dst = P.dst[cur.k] + cur.local * h;
     for (int64_t v = threadIdx.x; v < nvec; v += kCopyThreads) {
       const int64_t off = row * h + v * 8;
-      float y[8], q[8];
-      unpack8(ldg16_stream(P.src[0] + off), y);
-      for (int r = 1; r < t; ++r) {
-        unpack8(ldg16_stream(P.src[r] + off), q);
+      float y[8];
+      if constexpr (TT > 0) {
+        uint4 raw[TT];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], q[e]);
+        for (int r = 0; r < TT; ++r) raw[r] = ldg16_stream(P.src[r] + off);
+        unpack8(raw[0], y);
+#pragma unroll
+        for (int r = 1; r < TT; ++r) add8_bf16(raw[r], y);
+      } else {
+        unpack8(ldg16_stream(P.src[0] + off), y);
+        for (int rb = 1; rb < t; rb += 4) {
+          uint4 raw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (rb + i < t) raw[i] = ldg16_stream(P.src[rb + i] + off);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (rb + i < t) add8_bf16(raw[i], y);
+        }
       }
       st16_stream(dst + v * 8, pack8(y));
     }
@@ -95,7 +113,10 @@ cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_reduce_scatter(const CopyParams& p, int t, cudaStream_t st) {
-  reduce_scatter_kernel<<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p, t);
+  if (t == 8)
+    reduce_scatter_kernel<8><<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p, t);
+  else
+    reduce_scatter_kernel<0><<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p, t);
   return cudaGetLastError();
 }
 
