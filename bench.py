@@ -218,6 +218,13 @@ def profiled_traffic():
         return None
 
 
+def profiled_workload(args):
+    """The recorded traffic belongs to the default bench line only (70B shape,
+    LayerNorm, p = 0.1, one gathered copy, no size overrides)."""
+    return (args.workload == "70b" and not args.s and not args.h and args.p is None
+            and args.norm in (None, "layernorm") and args.n_gather == 1)
+
+
 class Step:
     """Device buffers and the fwd + bwd calls of one step.
 
@@ -525,6 +532,10 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     if args.s:
         w = w.with_(s=args.s, name=f"{w.name}-s{args.s}")
+    if args.h:
+        if w.ragged or args.h % 8:
+            raise SystemExit("--h: dense workloads only, a multiple of 8")
+        w = w.with_(h=args.h, name=f"{w.name}-h{args.h}")
     if args.p is not None:
         w = w.with_(p=args.p, name=f"{w.name}-p{args.p}")
     if args.norm is not None:
@@ -593,7 +604,8 @@ def run_ours(args):
                                "unfused forward (reduce_scatter + shard norm + allgather)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": profiled_traffic() if fused else None,
+                     "traffic": (profiled_traffic() if fused and profiled_workload(args)
+                                 else None),
                      "algorithmic_bytes": fb},
         "e2e": {"value": round(w.tokens * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -656,6 +668,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="70b", choices=["70b", "trace4k", "ragged", "tiny"])
     ap.add_argument("--s", type=int, default=0,
                     help="override the sequence length (smaller cases for profiling)")
+    ap.add_argument("--h", type=int, default=0,
+                    help="override the hidden size (dense workloads; a multiple of 8)")
     ap.add_argument("--p", type=float, default=None, help="override the dropout probability")
     ap.add_argument("--norm", choices=["layernorm", "rmsnorm"], default=None,
                     help="override the norm")
