@@ -298,6 +298,17 @@ def test_backward_70b_sampled_and_param_grads(name):
     C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
 
 
+def test_backward_ragged_workload_sampled_and_param_grads():
+    """The packed workload at full size in the bench's launch configuration
+    (h = 5120 runs the tensor-memory shape, 320 threads x 2 chunks):
+    sampled rows, including the first and last of every shard, and every
+    parameter gradient over all 42,823 tokens."""
+    w = wl.WORKLOADS["ragged"]
+    inp, fwd, b, out = _bwd_setup(w)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], None, out, C.sample_tokens(w, 96))
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
+
+
 def test_backward_deterministic():
     w = wl.Workload("det", t=4, b=1, s=512, h=2048, draw_seed=33)
     inp = wl.forward_inputs(w, C.DEV)
@@ -676,6 +687,32 @@ def test_rs_norm_bwd_70b_sampled():
     rng = np.random.default_rng(0)
     tokens = np.unique(np.concatenate([[0, 1, 2047], rng.integers(0, 2048, 40)]))
     _rs_bwd_check(w, fwd, inp, parts, None, out, tokens=tokens)
+
+
+@pytest.mark.parametrize("t,h,skip", [(2, 16384, False), (16, 8192, True)])
+def test_rs_norm_bwd_rejects_shapes_it_cannot_run(t, h, skip):
+    """h above 8192, and t = 16 at h = 8192 with a skip gradient (the t partial
+    stages and the row buffers do not fit one SM's shared memory), are
+    refused before anything is launched; outputs stay untouched."""
+    w = wl.Workload("rsx", t=t, b=1, s=2 * t, h=h, draw_seed=85)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(86, C.DEV)
+    parts = [torch.randn((1, w.s, w.h), generator=gen, device=C.DEV).to(torch.bfloat16)
+             for _ in range(w.t)]
+    sk = wl.backward_inputs(w, C.DEV, with_skip=True)["dz_skip"] if skip else None
+    out = C.alloc_bwd(w, 1)
+    for x in out["dres"] + out["dgat"]:
+        x.fill_(5.0)
+    torch.cuda.synchronize()
+    with pytest.raises(C.sp.SpError) as e:
+        C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"],
+                            inp["gamma"], sk, p=w.p, norm=w.norm, dresidual=out["dres"],
+                            dgathered=out["dgat"], dgamma=out["dgamma"], dbeta=out["dbeta"],
+                            dbias=out["dbias"], workspace=out["ws"])
+    assert e.value.name == "SP_ERR_UNSUPPORTED"
+    torch.cuda.synchronize()
+    assert all(bool((x.float() == 5.0).all()) for x in out["dres"] + out["dgat"])
 
 
 def test_rs_norm_bwd_equals_unfused_reduce_then_norm_bwd_within_rounding():
