@@ -43,6 +43,15 @@ bool take_injected(sp_status_t* out) {
   return true;
 }
 
+// An injected SP_ERR_TIMEOUT is not returned by the host: the next forward
+// launches with its device-side withhold hook set instead (block 0's copy
+// producer never stages its first chunk, so that block's waits run out and
+// the call's status word reads SP_ERR_TIMEOUT).
+bool take_injected_timeout() {
+  int expect = SP_ERR_TIMEOUT;
+  return g_inject.compare_exchange_strong(expect, SP_OK);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // A list of device byte ranges; outputs must not overlap anything else.
@@ -328,16 +337,17 @@ void bwd_threads(int64_t h, bool regen, int* threads, int* maxc) {
   *maxc = nvec <= 512 ? 1 : nvec <= 1024 ? 2 : 4;
 }
 
-// Forward: every thread owns 8 channels of each chunk of 8 * threads channels;
-// one pipeline stage holds the chunk of the t partials and the residual, and
-// the row's Z waits in shared memory for the statistics.
+// Forward: every compute thread owns 8 channels of each chunk of 8 * threads
+// channels, and the block adds one copy-producer warp; one pipeline stage
+// holds the chunk of the t partials and the residual, and the row's Z waits
+// in shared memory for the statistics.
 LaunchShape fwd_shape_uncached(int64_t rows, int64_t h, int t) {
   const int threads = fwd_threads(h);
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
   const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float2);
-  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 2,
-                    /*stages=*/3, /*blocks per SM=*/512 / threads,
+  return pick_shape(0, threads + kFwdProducerThreads, static_cast<int>(nchunk), rows, stage,
+                    fixed, kFwdStages, 2, /*stages=*/3, /*blocks per SM=*/512 / threads,
                     [&](int st) { return fwd_kernel(threads, t, st); });
 }
 
@@ -347,7 +357,8 @@ LaunchShape fwd_shard_shape_uncached(int64_t rows, int64_t h) {
   const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(2) * threads * 16;
   const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float2);
-  return pick_shape(0, threads, static_cast<int>(nchunk), rows, stage, fixed, kFwdStages, 2,
+  return pick_shape(0, threads + kFwdProducerThreads, static_cast<int>(nchunk), rows, stage,
+                    fixed, kFwdStages, 2,
                     /*stages=*/3, /*blocks per SM=*/512 / threads,
                     [&](int st) { return fwd_shard_kernel(threads, st); });
 }
@@ -483,6 +494,7 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
                            void* const* gathered, int32_t n_gather, int32_t* dev_status,
                            void* stream) {
   sp_status_t st;
+  const bool withhold = take_injected_timeout();
   if (take_injected(&st)) return st;
   if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
   if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
@@ -554,9 +566,10 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   P.off1 = static_cast<uint32_t>(offset >> 32);
   P.rows = rows;
   P.status = dev_status;
+  P.withhold = withhold ? 1 : 0;
 
   const LaunchShape ls = fwd_shape(rows, h, t);
-  const cudaError_t e = launch(fwd_kernel(ls.threads, t, ls.stages), ls, &P,
+  const cudaError_t e = launch(fwd_kernel(ls.threads - kFwdProducerThreads, t, ls.stages), ls, &P,
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_fwd launch");
   return SP_OK;
@@ -571,6 +584,7 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
                               float* const* rstd_out, void* const* o_shards,
                               int32_t* dev_status, void* stream) {
   sp_status_t st;
+  const bool withhold = take_injected_timeout();
   if (take_injected(&st)) return st;
   if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
   if (norm != SP_NORM_LAYERNORM && norm != SP_NORM_RMSNORM)
@@ -634,8 +648,9 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
   P.off1 = static_cast<uint32_t>(offset >> 32);
   P.rows = b * s;
   P.status = dev_status;
+  P.withhold = withhold ? 1 : 0;
   const LaunchShape ls = fwd_shard_shape(P.rows, h);
-  const cudaError_t e = launch(fwd_shard_kernel(ls.threads, ls.stages), ls, &P,
+  const cudaError_t e = launch(fwd_shard_kernel(ls.threads - kFwdProducerThreads, ls.stages), ls, &P,
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_shard_norm_fwd launch");
   return SP_OK;

@@ -8,21 +8,29 @@
 // of that token once, and writes Z, the mask, the statistics and the
 // normalised row straight into the all-gather destination(s).
 //
-// Work layout: a persistent grid (16 warps per SM); block b of G processes
-// tokens b, b + G, b + 2G, ... when every block gets at least 32 rows (the
-// blocks then stream neighbouring rows together: 0.7 % faster on the 70B
-// shape), else a contiguous range of about rows/G tokens; either way the walk
-// moves the shard and the row inside it by increments (no per-row division or
-// shard search).  A row of h channels is cut into chunks of 8*T
-// channels (T = threads); in each chunk thread i owns channels [8i, 8i+8).
-// Every thread streams its own 16-byte pieces of the t + 1 input rows into
-// its own shared-memory slots with cp.async, STAGES - 1 chunks ahead, so the
-// loads of the next chunks are in flight while the current one is summed,
-// dropped out, normalised and stored.  A thread only reads back what it
-// copied itself, so the pipeline needs no block barrier; the only barriers
-// are the row reductions of the norm.  The chunk loop is not unrolled (the
-// Philox rounds make its body long): Z of the row waits for the statistics
-// in the thread's own shared-memory slots rather than in registers.
+// Work layout: a persistent grid (16 compute warps per SM); block b of G
+// processes tokens b, b + G, b + 2G, ... when every block gets at least 32
+// rows (the blocks then stream neighbouring rows together), else a
+// contiguous range of about rows/G tokens; either way the walk moves the
+// shard and the row inside it by increments (no per-row division or shard
+// search).  A row of h channels is cut into chunks of 8*T channels (T =
+// compute threads); in each chunk thread i owns channels [8i, 8i+8).
+//
+// Staging: one extra warp per block is the copy producer.  For every (row,
+// chunk) item in order it waits until the compute warps have released the
+// item's stage (an mbarrier each warp arrives on once it has read the stage),
+// then arms the stage's "full" mbarrier with the item's byte count and issues
+// one bulk global -> shared copy per input stream (the t partial rows and the
+// residual row of the chunk, cp.async.bulk completing on that mbarrier).  The
+// compute warps wait on "full", read their own 16 bytes of every stream, sum
+// the partials, release the stage at once and only then run the dropout and
+// the rest, so the next chunks are in flight while a chunk is computed.  The
+// only block-wide barriers are the row reductions of the norm, on a named
+// barrier of the compute warps.  Every wait is bounded (about a second of
+// %globaltimer, then SP_ERR_TIMEOUT in the status word and no further waits).
+// The chunk loop is not unrolled (the Philox rounds make its body long): Z of
+// the row waits for the statistics in the thread's own shared-memory slots
+// rather than in registers.
 #include "fwd_kernel.cuh"
 
 namespace spb {

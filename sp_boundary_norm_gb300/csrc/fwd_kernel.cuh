@@ -6,8 +6,8 @@
 
 namespace spb {
 
-// Blocks are sized for 16 resident warps per SM: 512 / NTHR blocks of NTHR
-// threads (at most 128 registers per thread).
+// Blocks are sized for 16 resident compute warps per SM: 512 / NTHR blocks of
+// NTHR compute threads plus one copy-producer warp.
 // SHARD = false: the fused boundary (inputs: the t full partials; output:
 // the gathered full buffers).  SHARD = true: the middle step of the unfused
 // boundary (input: each rank's already reduced shard, one stream; output: O
@@ -15,10 +15,13 @@ namespace spb {
 // pointers).  Dropout draws use the token's index in the full sequence in
 // both cases.
 template <int NTHR, int STAGES, int TT, bool SHARD>
-__global__ void __launch_bounds__(NTHR, 512 / NTHR)
+__global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     rs_norm_fwd_kernel(const FwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
+  constexpr int kWarps = NTHR / 32;   // compute warps; warp kWarps issues the copies
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
   // input streams summed per element (compile-time when specialised)
   const int t = SHARD ? 1 : (TT > 0 ? TT : P.map.t);
   const int64_t h = P.map.h;
@@ -30,9 +33,16 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
   float2* red = reinterpret_cast<float2*>(smem + STAGES * stage_bytes + nchunk * kStream);   // [2][32]
   const bool is_ln = (P.norm == SP_NORM_LAYERNORM);
 
+  if (tid == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], kWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
-  // this block's rows: a contiguous range
   // this block's rows: every G-th token from blockIdx.x when blocks get many
   // rows (neighbouring tokens are then in flight together), else a
   // contiguous range
@@ -48,49 +58,60 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
   }
   const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
 
-  // ---- prefetch cursor: the next (row, chunk) item to stage -------------
-  // pf_goff: element offset of (row, chunk) in the (b, s, h) partials;
-  // pf_roff: element offset in the residual shard of that row.
-  RowWalk pf;
-  pf.init(P.map, r0);
-  int64_t pf_ri = 0, pf_goff = pf.row * h + c0, pf_roff = pf.local * h + c0;
-  int pf_chunk = 0, pf_stage = 0;
-
-  auto issue_next = [&]() {
-    if (pf_ri < nrows) {
-      if (pf_chunk * kChunk + c0 < h) {
-        uint8_t* slot = smem + pf_stage * stage_bytes + tid * 16;
-        if (SHARD) {
-          cp_async16(slot, P.partials[pf.k] + pf_roff);
-        } else {
+  // ---- producer warp: stage every (row, chunk) item in order ------------
+  // Item j goes to stage j % STAGES as soon as the compute warps have
+  // released the stage's previous item (they do so right after reading it,
+  // so a stage refills while the previous chunk is still being computed);
+  // lane 0 arms the stage's full barrier with the item's byte count and
+  // issues one bulk copy per stream.  After a wait times out a thread stops
+  // waiting (its later data may be wrong; the call reports SP_ERR_TIMEOUT),
+  // so a broken pipeline costs about one wait limit, not one per item.
+  bool timed_out = false;
+  if (tid >= NTHR) {
+    RowWalk pf;
+    pf.init(P.map, r0);
+    int64_t item = 0;
+    for (int64_t ri = 0; ri < nrows; ++ri) {
+      if (ri > 0) pf.next(P.map, step);
+      const int64_t goff = pf.row * h, roff = pf.local * h;
+      const int kk = pf.k;
+      for (int ch = 0; ch < nchunk; ++ch, ++item) {
+        const int s = static_cast<int>(item % STAGES);
+        const int64_t use = item / STAGES;
+        if (use > 0 && !timed_out &&
+            !mbar_wait(&bar_empty[s], static_cast<uint32_t>((use - 1) & 1)))
+          timed_out = true;
+        const bool withheld = P.withhold != 0 && blockIdx.x == 0 && item == 0;   // test hook
+        if (lane == 0 && !withheld) {
+          const int cc = ch * kChunk;
+          const int n = (h - cc < kChunk) ? static_cast<int>(h - cc) : kChunk;
+          const uint32_t bytes = static_cast<uint32_t>(n) * 2u;
+          uint8_t* dst = smem + s * stage_bytes;
+          mbar_arrive_expect_tx(&bar_full[s], bytes * static_cast<uint32_t>(t + 1));
+          if (SHARD) {
+            bulk_g2s(dst, P.partials[kk] + roff + cc, bytes, &bar_full[s]);
+          } else {
 #pragma unroll
-          for (int r = 0; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
-            if (TT > 0 || r < t) cp_async16(slot + r * kStream, P.partials[r] + pf_goff);
+            for (int r = 0; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
+              if (TT > 0 || r < t) bulk_g2s(dst + r * kStream, P.partials[r] + goff + cc, bytes,
+                                            &bar_full[s]);
+          }
+          bulk_g2s(dst + t * kStream, P.residual[kk] + roff + cc, bytes, &bar_full[s]);
         }
-        cp_async16(slot + t * kStream, P.residual[pf.k] + pf_roff);
-      }
-      if (++pf_chunk == nchunk) {
-        pf_chunk = 0;
-        if (++pf_ri < nrows) {
-          pf.next(P.map, step);
-          pf_goff = pf.row * h + c0;
-          pf_roff = pf.local * h + c0;
-        }
-      } else {
-        pf_goff += kChunk;
-        pf_roff += kChunk;
+        __syncwarp();
       }
     }
-    cp_async_commit();
-    pf_stage = (pf_stage + 1 == STAGES) ? 0 : pf_stage + 1;
-  };
-
-#pragma unroll
-  for (int i = 0; i < STAGES - 1; ++i) issue_next();
+    // the last copies must land before the block may end (bounded even
+    // after a timeout)
+    for (int64_t j = (item > STAGES ? item - STAGES : 0); j < item; ++j)
+      if (!mbar_wait(&bar_full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1)))
+        timed_out = true;
+    if (timed_out && P.status != nullptr) *P.status = SP_ERR_TIMEOUT;
+    return;
+  }
 
   RowWalk cur;
   cur.init(P.map, r0);
-  int stage = 0;
   int slot_sel = 0;
   const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
@@ -106,21 +127,29 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
     float lsum = 0.f, lsq = 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < nchunk; ++ch) {
-      issue_next();
-      cp_async_wait<STAGES - 1>();
+      const int64_t item = ri * nchunk + ch;
+      const int stage = static_cast<int>(item % STAGES);
+      if (!timed_out && !mbar_wait(&bar_full[stage], static_cast<uint32_t>((item / STAGES) & 1)))
+        timed_out = true;
       const int cc = ch * kChunk;
+      // g*: float32 sum of the t partials, ranks in ascending order
+      // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
+      float y[8];
+      uint4 rv = make_uint4(0, 0, 0, 0);
       if (cc + c0 < h) {
         const uint8_t* slot = smem + stage * stage_bytes + tid * 16;
-        const uint4 bv = ldg16(P.bias + cc + c0);
-        // g*: float32 sum of the t partials, ranks in ascending order
-        // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
-        float y[8];
         unpack8(lds16(slot), y);
         if (!SHARD) {
 #pragma unroll
           for (int r = 1; r < (TT > 0 ? TT : SP_MAX_RANKS); ++r)
             if (TT > 0 || r < t) add8_bf16(lds16(slot + r * kStream), y);
         }
+        rv = lds16(slot + t * kStream);   // the residual, used after the dropout
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_empty[stage]);   // the stage is free again
+      if (cc + c0 < h) {
+        const uint4 bv = ldg16(P.bias + cc + c0);
         add8_bf16(bv, y);   // + bias
         // dropout: element e keeps iff its Philox word >= thr
         uint2 keep = make_uint2(0x01010101u, 0x01010101u);
@@ -142,7 +171,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
           keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         }
         // (with p == 0 the scale is exactly 1 and y * 1 == y)
-        add8_bf16(lds16(slot + t * kStream), y);   // + residual -> Z in fp32
+        add8_bf16(rv, y);                           // + residual -> Z in fp32
         const uint4 zb = pack8(y);                 // Z = bf16_rne(...)
         st16_stream(zrow + cc, zb);
         st8_stream(mrow + cc, keep);
@@ -164,7 +193,6 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
           lsum += l2[0] + l2[1];
         }
       }
-      stage = (stage + 1 == STAGES) ? 0 : stage + 1;
     }
 
     // ---- token-wise statistics over h ------------------------------------
@@ -176,7 +204,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
     // in a second pass as the mean of (Z - mean)^2.
     float mean = 0.f, rstd;
     if (is_ln) {
-      const float2 sums = block_sum2(lsum, lsq, red + 32 * slot_sel);
+      const float2 sums = warps_sum2<kWarps>(lsum, lsq, red + 32 * slot_sel);
       slot_sel ^= 1;
       mean = sums.x * inv_h;
       const float var1 = sums.y * inv_h - mean * mean;
@@ -194,12 +222,12 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
             for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
           }
         }
-        const float var = block_sum(lsqa + lsqb, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
+        const float var = warps_sum<kWarps>(lsqa + lsqb, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
         slot_sel ^= 1;
         rstd = rsqrtf(var + P.eps);
       }
     } else {
-      const float ms = block_sum(lsq, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
+      const float ms = warps_sum<kWarps>(lsq, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
       slot_sel ^= 1;
       rstd = rsqrtf(ms + P.eps);
     }
@@ -243,7 +271,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR)
       P.rstd[k][local] = rstd;
     }
   }
-  cp_async_wait<0>();
+  if (timed_out && P.status != nullptr) *P.status = SP_ERR_TIMEOUT;
 }
 
 }  // namespace spb

@@ -263,6 +263,73 @@ __device__ __forceinline__ void st8_stream(void* p, uint2 v) {
   __stcs(reinterpret_cast<uint2*>(p), v);
 }
 
+// ------------------------------------------- bulk copies and mbarriers --
+// The forward stages its inputs with bulk global -> shared copies issued by
+// one producer warp and completed on mbarriers (transaction counts), the
+// consumer warps releasing each stage through a second mbarrier.  Every wait
+// is bounded: it gives up after kWaitLimitNs of %globaltimer and the caller
+// reports SP_ERR_TIMEOUT instead of hanging.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count)
+               : "memory");
+}
+
+// Makes the initialised mbarriers visible to the copy engine and the block.
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+// One arrival that also announces `bytes` of copies completing on b.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase of b with the given parity has completed; false if
+// that takes longer than kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(b, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// One contiguous global -> shared copy (16-byte aligned ends, a multiple of
+// 16 bytes), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------ tensor memory --
 // Tensor memory (TMEM, 128 lanes x 512 columns of 32 bits per SM) used as
 // per-thread accumulator storage: warp w reaches lanes 32*(w % 4) .. +31, one
@@ -377,6 +444,34 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
   if (lane == 0) red[warp] = make_float2(a, b);
   __syncthreads();
   const float2 p = lane < nw ? red[lane] : make_float2(0.f, 0.f);
+  return make_float2(warp_sum(p.x), warp_sum(p.y));
+}
+
+// Block sums over the first NW warps only, synchronised on named barrier 1
+// (a block whose last warp runs a copy producer that never joins them); same
+// order and bits as block_sum / block_sum2 over a block of NW warps.
+template <int NW>
+__device__ __forceinline__ void warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
+}
+
+template <int NW>
+__device__ __forceinline__ float warps_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  warps_sync<NW>();
+  return warp_sum(lane < NW ? red[lane] : 0.f);
+}
+
+template <int NW>
+__device__ __forceinline__ float2 warps_sum2(float a, float b, float2* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (lane == 0) red[warp] = make_float2(a, b);
+  warps_sync<NW>();
+  const float2 p = lane < NW ? red[lane] : make_float2(0.f, 0.f);
   return make_float2(warp_sum(p.x), warp_sum(p.y));
 }
 

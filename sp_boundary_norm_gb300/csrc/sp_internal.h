@@ -55,6 +55,9 @@ struct ShardMap {
   int32_t t;
 };
 
+// The forward's blocks add one copy-producer warp to their compute threads.
+constexpr int kFwdProducerThreads = 32;
+
 struct FwdParams {
   ShardMap map;
   const uint16_t* partials[SP_MAX_RANKS];
@@ -75,6 +78,7 @@ struct FwdParams {
   float scale;           // float(1/(1-p))
   float eps;
   PhiloxKeys rk;         // Philox round keys of the seed
+  int32_t withhold;      // test hook: block 0 never stages its first chunk
   uint32_t off0, off1;   // Philox counter words 2, 3 = offset
   int64_t rows;          // b * s
   int32_t* status;

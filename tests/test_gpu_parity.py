@@ -246,6 +246,30 @@ def test_injected_failure_launches_nothing():
     C.run_fwd(w, inp, out=out)                                           # hook disarmed
 
 
+def test_forward_bounded_wait_reports_timeout():
+    """The SP_ERR_TIMEOUT test hook makes block 0's copy producer withhold its
+    first chunk: that block's bounded waits give up after about a second, the
+    status word reads SP_ERR_TIMEOUT, nothing hangs or faults, and the next
+    call is exact again."""
+    import time
+    w = wl.Workload("to", t=2, b=1, s=64, h=512, draw_seed=121)
+    inp = wl.forward_inputs(w, C.DEV)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.sp.sp_debug_inject(5)                                            # SP_ERR_TIMEOUT
+    t0 = time.perf_counter()
+    C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0
+    with pytest.raises(C.sp.SpError) as e:
+        C.sp.check_device_status(C.DEV)
+    assert e.value.name == "SP_ERR_TIMEOUT"
+    out = C.run_fwd(w, inp)                                            # hook disarmed
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    _full_fwd_compare(w, inp, out)
+
+
 # ------------------------------------------------------------------ backward
 
 def _bwd_setup(w, with_skip=False, n_gather=1):
