@@ -92,3 +92,17 @@ def test_backward_through_g_byte_counts():
     assert bench.bwd_g_bytes_per_token(t, h, 1, fused=False) == 27 * h + 8
     # reduce-scatter 18h, shard norm 9h + 8, all-gather 4h
     assert bench.unfused_fwd_bytes_per_token(t, h, 1) == 31 * h + 8
+
+
+def test_recorded_traffic_only_on_the_profiled_workload():
+    """roofline.traffic comes from the ncu summary of the default line; any
+    other workload, size or norm reports null."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args([])
+    assert bench.profiled_workload(args)
+    for extra in (["--h", "5120"], ["--s", "4096"], ["--norm", "rmsnorm"], ["--p", "0"],
+                  ["--n-gather", "8"], ["--workload", "ragged"], ["--workload", "trace4k"]):
+        assert not bench.profiled_workload(bench.parse_args(extra)), extra
+    assert bench.profiled_workload(bench.parse_args(["--norm", "layernorm"]))
