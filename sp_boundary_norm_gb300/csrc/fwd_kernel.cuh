@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
           keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         }
         // (with p == 0 the scale is exactly 1 and y * 1 == y)
-        add8_bf16(rv, y);                           // + residual -> Z in fp32
+        add8_bf16(rv, y);   // + residual -> Z in fp32
         const uint4 zb = pack8(y);                 // Z = bf16_rne(...)
         st16_stream(zrow + cc, zb);
         st8_stream(mrow + cc, keep);

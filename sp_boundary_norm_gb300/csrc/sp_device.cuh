@@ -129,13 +129,6 @@ __device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t b, float& c0, flo
       : "r"(a), "r"(b));
 }
 
-__device__ __forceinline__ void fma8_bf16(const uint4 a, const uint4 b, float c[8]) {
-  fma2_bf16(a.x, b.x, c[0], c[1]);
-  fma2_bf16(a.y, b.y, c[2], c[3]);
-  fma2_bf16(a.z, b.z, c[4], c[5]);
-  fma2_bf16(a.w, b.w, c[6], c[7]);
-}
-
 // ------------------------------------------------- packed fp32 (f32x2) --
 // sm_100-class packed fp32 arithmetic: two independent IEEE fp32 operations
 // (round to nearest even, no fusion beyond what is written) in one
@@ -425,18 +418,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Block-wide sums in a fixed order (deterministic): warp butterflies, one
-// partial per warp in shared memory, then every warp runs the same butterfly
-// over those partials, so all threads get the same bits.  `red` is a
-// 32-entry shared slot; two consecutive calls must use different slots.
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_sum(v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  return warp_sum(lane < nw ? red[lane] : 0.f);
-}
-
+// Two block-wide sums in a fixed order (deterministic): warp butterflies,
+// one partial pair per warp in shared memory, then every warp runs the same
+// butterfly over those partials, so all threads get the same bits.  `red` is
+// a 32-entry shared slot; two consecutive calls must use different slots.
 __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   a = warp_sum(a);
@@ -449,7 +434,7 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 
 // Block sums over the first NW warps only, synchronised on named barrier 1
 // (a block whose last warp runs a copy producer that never joins them); same
-// order and bits as block_sum / block_sum2 over a block of NW warps.
+// order and bits as block_sum2 over a block of NW warps.
 template <int NW>
 __device__ __forceinline__ void warps_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
