@@ -53,7 +53,11 @@ typedef enum sp_status {
   SP_ERR_UNSUPPORTED = 3,   /* valid request outside this build (h > SP_MAX_HIDDEN, or no
                                launch shape of the kernel fits one SM's shared memory) */
   SP_ERR_CUDA = 4,          /* a CUDA runtime error (text in sp_last_error) */
-  SP_ERR_TIMEOUT = 5,       /* a bounded device-side wait expired (via dev_status) */
+  SP_ERR_TIMEOUT = 5,       /* a bounded device-side wait expired (via dev_status): the
+                               forward's staging waits give up after about a second of
+                               wall time (also if the context was preempted that long
+                               mid-kernel); the call's outputs are then undefined and
+                               the call may simply be repeated */
   SP_ERR_DEVICE_CHECK = 6,  /* device-side validation failed (via dev_status) */
   SP_ERR_OVERLAP = 7        /* an output buffer overlaps another buffer */
 } sp_status_t;
