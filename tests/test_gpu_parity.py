@@ -56,6 +56,35 @@ def test_forward_full_compare(name):
     _full_fwd_compare(w, inp, out)
 
 
+@pytest.mark.parametrize("variant", [dict(), dict(b=2, s=36, t=3), dict(norm="rmsnorm", eps=1e-6)])
+def test_forward_equals_unsharded_path_sliced_by_token(variant):
+    """Sequence parallelism leaves every token-wise result unchanged: the GPU
+    boundary equals the TP-only path (all-reduce of the partials, then bias,
+    dropout, residual and the norm on every token) sliced by shard; Z and the
+    mask bit for bit, the statistics and O within the stated tolerances."""
+    w = wl.Workload("us", t=4, b=1, s=64, h=1024, draw_seed=131).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
+    residual_full = np.concatenate([C.f32(r) for r in inp["residual"]], axis=1)
+    ref = ob.unsharded_fwd([C.f32(x) for x in inp["partials"]], residual_full,
+                           C.f32(inp["bias"]), C.f32(inp["gamma"]), C.f32(inp["beta"]),
+                           eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm)
+    for k in range(w.t):
+        sl = slice(offs[k], offs[k + 1])
+        assert np.array_equal(compare.bf16_bits(out["z"][k]), compare.bf16_bits(ref["z"][:, sl])), k
+        assert np.array_equal(out["mask"][k].cpu().numpy(), ref["mask"][:, sl]), k
+        assert not compare.f32_rel_mismatch(out["rstd"][k].cpu().numpy(), ref["rstd"][:, sl]).any()
+        if w.norm == "layernorm":
+            assert not compare.f32_rel_mismatch(out["mean"][k].cpu().numpy(),
+                                                ref["mean"][:, sl]).any()
+    bad = compare.bf16_mismatch(compare.bf16_bits(out["gathered"][0]), ref["out_exact"],
+                                ref["out_magnitude"])
+    assert not bad.any(), f"{bad.sum()} elements off"
+
+
 def test_layernorm_rows_with_large_mean():
     """The forward takes the LayerNorm variance as E[Z^2] - mean^2 only where
     mean^2 <= var / 4 and recomputes it from (Z - mean)^2 elsewhere.  Residual
