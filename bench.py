@@ -319,11 +319,17 @@ def capture(fn, device):
     return g.replay
 
 
+B2B_CALLS = 8   # calls per graph in the back-to-back loops
+
+
 def time_device(step, steps, warmup, world, device, launch="graph"):
-    """K steps between two events (the headline), then K more with events
-    between each step's forward and backward (the per-call split).  With
-    `launch` "graph" a step is one CUDA graph holding its forward and backward
-    calls, and the split loop replays one graph per call."""
+    """K steps between two events (the headline); then K more with events
+    between each step's forward and backward (the per-call split); then K
+    forward calls and K backward calls, B2B_CALLS back to back per graph with
+    one event pair around each run of graphs (the per-launch duration, without
+    the gap an event pair leaves around every graph launch).  With `launch`
+    "graph" a step is one CUDA graph holding its forward and backward calls,
+    and the split loop replays one graph per call."""
     stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
         step.fwd()
@@ -331,14 +337,21 @@ def time_device(step, steps, warmup, world, device, launch="graph"):
     torch.cuda.synchronize(device)
     fwd, bwd = step.fwd, step.bwd
     whole = lambda: (step.fwd(), step.bwd())
+    fwd_run = lambda: [step.fwd() for _ in range(B2B_CALLS)]
+    bwd_run = lambda: [step.bwd() for _ in range(B2B_CALLS)]
     if launch == "graph":
         fwd, bwd = capture(step.fwd, device), capture(step.bwd, device)
         whole = capture(lambda: (step.fwd(), step.bwd()), device)
+        fwd_run, bwd_run = capture(fwd_run, device), capture(bwd_run, device)
         for _ in range(warmup):
             whole()
             fwd()
             bwd()
+        fwd_run()
+        bwd_run()
         torch.cuda.synchronize(device)
+    runs = max(1, steps // B2B_CALLS)
+    b2b = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     start, end = (torch.cuda.Event(enable_timing=True) for _ in range(2))
     sampler = ClockSampler(device)
@@ -358,6 +371,14 @@ def time_device(step, steps, warmup, world, device, launch="graph"):
         bwd()
         ev[k][2].record(stream)
     torch.cuda.synchronize(device)
+    b2b[0].record(stream)
+    for _ in range(runs):
+        fwd_run()
+    b2b[1].record(stream)
+    for _ in range(runs):
+        bwd_run()
+    b2b[2].record(stream)
+    torch.cuda.synchronize(device)
     t1 = time.time()
     barrier(world, device)
     sampler.stop()
@@ -365,7 +386,10 @@ def time_device(step, steps, warmup, world, device, launch="graph"):
     total_ms = start.elapsed_time(end)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    return total_ms, fwd_ms, bwd_ms, sampler.summary(t0, t1)
+    n = runs * B2B_CALLS
+    back_to_back = {"calls": n, "fwd_ms": b2b[0].elapsed_time(b2b[1]) / n,
+                    "bwd_ms": b2b[1].elapsed_time(b2b[2]) / n}
+    return total_ms, fwd_ms, bwd_ms, back_to_back, sampler.summary(t0, t1)
 
 
 def time_e2e(step_a, step_b, steps, device):
@@ -543,13 +567,13 @@ def run_ours(args):
                     name=f"{w.name}-{args.norm}")
     step = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
                 bwd_entry=args.bwd_entry)
-    total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world, device,
-                                                   args.launch)
+    total_ms, fwd_ms, bwd_ms, b2b, clocks = time_device(step, args.steps, args.warmup, world,
+                                                        device, args.launch)
     rejected = False
     if clocks_rejected(clocks):
         rejected = True
-        total_ms, fwd_ms, bwd_ms, clocks = time_device(step, args.steps, args.warmup, world,
-                                                       device, args.launch)
+        total_ms, fwd_ms, bwd_ms, b2b, clocks = time_device(step, args.steps, args.warmup,
+                                                            world, device, args.launch)
     total_ms = max_over_ranks(total_ms, world, device)
     tokens = w.tokens * args.steps * world
     value = tokens / (total_ms / 1e3)
@@ -565,7 +589,7 @@ def run_ours(args):
     bwd_avg = statistics.mean(bwd_ms)
     peak, peak_kind = measured_peak()
     step_ms = total_ms / args.steps
-    achieved = fb / (fwd_avg / 1e3) / 1e9
+    achieved = fb / (b2b["fwd_ms"] / 1e3) / 1e9
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     step_b = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
                   bwd_entry=args.bwd_entry)
@@ -595,15 +619,21 @@ def run_ours(args):
         "hbm_gbs": round((fb + bb) / (step_ms / 1e3) / 1e9, 1),
         "hbm_frac_of_peak": round((fb + bb) / (step_ms / 1e3) / 1e9 / peak, 4),
         "hbm_frac_of_nominal": round((fb + bb) / (step_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
-        "fwd": {"ms": round(fwd_avg, 4), "gbs": round(achieved, 1),
-                "bytes": fb, "tokens_per_s": round(w.tokens / (fwd_avg / 1e3), 1)},
+        "fwd": {"ms": round(fwd_avg, 4), "gbs": round(fb / (fwd_avg / 1e3) / 1e9, 1),
+                "bytes": fb, "tokens_per_s": round(w.tokens / (fwd_avg / 1e3), 1),
+                "ms_back_to_back": round(b2b["fwd_ms"], 4)},
         "bwd": {"ms": round(bwd_avg, 4), "gbs": round(bb / (bwd_avg / 1e3) / 1e9, 1),
-                "bytes": bb, "tokens_per_s": round(w.tokens / (bwd_avg / 1e3), 1)},
+                "bytes": bb, "tokens_per_s": round(w.tokens / (bwd_avg / 1e3), 1),
+                "ms_back_to_back": round(b2b["bwd_ms"], 4),
+                "gbs_back_to_back": round(bb / (b2b["bwd_ms"] / 1e3) / 1e9, 1)},
         "roofline": {"bound": "hbm",
                      "kernel": "rs_norm_fwd_kernel" if fused else
                                "unfused forward (reduce_scatter + shard norm + allgather)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "launch_ms": round(b2b["fwd_ms"], 4),
+                     "timing": f"{b2b['calls']} forward calls, {B2B_CALLS} back to back per "
+                               "graph replay, one event pair around all of them",
                      "traffic": (profiled_traffic() if fused and profiled_workload(args)
                                  else None),
                      "algorithmic_bytes": fb},
