@@ -319,7 +319,8 @@ def capture(fn, device):
     return g.replay
 
 
-B2B_CALLS = 8   # calls per graph in the back-to-back loops
+B2B_CALLS = 8    # calls per graph in the back-to-back loops
+GRAPH_STEPS = 8  # whole steps per graph in the headline loop
 
 
 def time_device(step, steps, warmup, world, device, launch="graph"):
@@ -328,23 +329,32 @@ def time_device(step, steps, warmup, world, device, launch="graph"):
     forward calls and K backward calls, B2B_CALLS back to back per graph with
     one event pair around each run of graphs (the per-launch duration, without
     the gap an event pair leaves around every graph launch).  With `launch`
-    "graph" a step is one CUDA graph holding its forward and backward calls,
-    and the split loop replays one graph per call."""
+    "graph" the headline loop replays CUDA graphs of GRAPH_STEPS whole steps
+    (each step its forward and backward calls; the last graph takes the
+    remainder, so exactly K steps run), as a training iteration captured in
+    one graph would run them, and the split loop replays one graph per
+    call."""
     stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
         step.fwd()
         step.bwd()
     torch.cuda.synchronize(device)
     fwd, bwd = step.fwd, step.bwd
-    whole = lambda: (step.fwd(), step.bwd())
+    one_step = lambda: (step.fwd(), step.bwd())
+    steps_of = lambda n: (lambda: [one_step() for _ in range(n)])
+    per_graph = max(1, min(GRAPH_STEPS, steps))
+    headline = [one_step] * steps
     fwd_run = lambda: [step.fwd() for _ in range(B2B_CALLS)]
     bwd_run = lambda: [step.bwd() for _ in range(B2B_CALLS)]
     if launch == "graph":
         fwd, bwd = capture(step.fwd, device), capture(step.bwd, device)
-        whole = capture(lambda: (step.fwd(), step.bwd()), device)
+        full = capture(steps_of(per_graph), device)
+        headline = [full] * (steps // per_graph)
+        if steps % per_graph:
+            headline.append(capture(steps_of(steps % per_graph), device))
         fwd_run, bwd_run = capture(fwd_run, device), capture(bwd_run, device)
         for _ in range(warmup):
-            whole()
+            full()
             fwd()
             bwd()
         fwd_run()
@@ -360,8 +370,8 @@ def time_device(step, steps, warmup, world, device, launch="graph"):
     torch.cuda.synchronize(device)
     t0 = time.time()
     start.record(stream)
-    for _ in range(steps):
-        whole()
+    for g in headline:
+        g()
     end.record(stream)
     torch.cuda.synchronize(device)
     for k in range(steps):
@@ -611,8 +621,9 @@ def run_ours(args):
                    "t": w.t, "b": w.b, "s": w.s, "h": w.h, "norm": w.norm, "p": w.p,
                    "n_gather": args.n_gather, "pipeline": args.pipeline,
                    "backward_mask": args.mask, "backward_entry": args.bwd_entry,
-                   "launch": "one cuda graph per step (its forward and backward calls); the "
-                             "fwd/bwd split from a second loop with one graph per call"
+                   "launch": f"cuda graphs of {min(GRAPH_STEPS, args.steps)} steps (each step "
+                             "its forward and backward calls); the fwd/bwd split from a second "
+                             "loop with one graph per call"
                              if args.launch == "graph" else "eager API calls",
                    "l2": "inputs larger than L2 (2.1 GB of partials per step), no flush",
                    "parallelism": f"replicas x{world} (independent batches)"},
