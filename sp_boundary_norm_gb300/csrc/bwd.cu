@@ -44,16 +44,22 @@ __global__ void __launch_bounds__(32 * kReduceWarps) param_reduce_kernel(const P
   if (c < P.h) {
     const float* src = P.ws + q * P.h + c;
     int b = warp;
-    // four independent loads in flight per step
-    for (; b + 3 * kReduceWarps < P.nblk; b += 4 * kReduceWarps) {
-      const float v0 = src[b * stride];
-      const float v1 = src[(b + kReduceWarps) * stride];
-      const float v2 = src[(b + 2 * kReduceWarps) * stride];
-      const float v3 = src[(b + 3 * kReduceWarps) * stride];
-      acc += v0;
-      acc += v1;
-      acc += v2;
-      acc += v3;
+    // eight, then four independent loads in flight per step; the adds keep
+    // the order b = w, w + 8, w + 16, ...
+    for (; b + 7 * kReduceWarps < P.nblk; b += 8 * kReduceWarps) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = src[(b + j * kReduceWarps) * stride];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+    if (b + 3 * kReduceWarps < P.nblk) {
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = src[(b + j * kReduceWarps) * stride];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc += v[j];
+      b += 4 * kReduceWarps;
     }
     for (; b < P.nblk; b += kReduceWarps) acc += src[b * stride];
   }
