@@ -165,7 +165,6 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
         float xh[8], dxh[8], dy[8];
         add8_bf16_bcast(zv, nmean, xh);             // z - mean
         fma8_bf16_bcast(dyv, gam[ch], 0.f, dxh);    // dY * gamma
-        if (is_ln) add8_bf16(dyv, gb + 8);          // dbeta terms
         unpack8(dyv, dy);
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
@@ -173,6 +172,7 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
           add2(s1a, s1b, dxh[e], dxh[e + 1]);
           fma2(s2a, s2b, dxh[e], dxh[e + 1], xh[e], xh[e + 1]);
           fma2(gb[e], gb[e + 1], dy[e], dy[e + 1], xh[e], xh[e + 1]);
+          if (is_ln) add2(gb[8 + e], gb[9 + e], dy[e], dy[e + 1]);   // dbeta terms
         }
       }
       if constexpr (TACC) {
