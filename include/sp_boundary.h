@@ -325,8 +325,11 @@ sp_status_t sp_debug_inject(sp_status_t code);
  * forward (kernel 0) or backward (kernel 1) row kernels: `stages` = cp.async
  * pipeline depth, `blocks_per_sm` = resident blocks per SM the grid is sized
  * for, `threads` = threads per block (forward: 64, 128, 160 or 256), `chunks`
- * = chunks per row (backward, with `threads`: one of the instantiated pairs);
- * 0 keeps the default rule for that field.  Values that do not fit shared
+ * = chunks per row (backward, with `threads`: one of the instantiated pairs;
+ * forward: 2 splits every token row over a thread-block cluster of two CTAs
+ * of h / 2 channels each, which exchange their parts of the row sums through
+ * distributed shared memory -- taken when h % 16 == 0 and the CTA has 128 or
+ * 256 threads, else ignored); 0 keeps the default rule for that field.  Values that do not fit shared
  * memory are reduced; shapes that are not instantiated are ignored.  Affects
  * sp_norm_bwd_workspace_bytes, so set it before sizing the workspace.  Results
  * do not depend on it except the float rounding of sums whose partition
@@ -335,6 +338,17 @@ sp_status_t sp_debug_inject(sp_status_t code);
  */
 sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm,
                           int32_t threads, int32_t chunks);
+
+/*
+ * sp_debug_last_shape -- test hook: the launch shape of the calling thread's
+ * last sp_rs_norm_fwd (kernel 0) or backward (kernel 1: sp_norm_bwd,
+ * sp_norm_bwd_philox, sp_norm_bwd_noalloc, sp_rs_norm_bwd) call, whether or
+ * not it launched.  out: host int32 [6] = compute threads per block, chunks
+ * per row (backward) or row chunks of one CTA (forward), pipeline stages,
+ * grid (blocks), CTAs per cluster, dynamic shared memory bytes; all zero
+ * before the first call.
+ */
+sp_status_t sp_debug_last_shape(int32_t kernel, int32_t* out);
 
 /*
  * sp_debug_philox -- evaluate the library's device Philox4x32-10 on n

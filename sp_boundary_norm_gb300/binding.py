@@ -83,6 +83,8 @@ def load():
     lib.sp_debug_inject.argtypes = [_i32]
     lib.sp_debug_tune.restype = _i32
     lib.sp_debug_tune.argtypes = [_i32, _i32, _i32, _i32, _i32]
+    lib.sp_debug_last_shape.restype = _i32
+    lib.sp_debug_last_shape.argtypes = [_i32, _vp]
     lib.sp_debug_philox.restype = _i32
     lib.sp_debug_philox.argtypes = [_vp, _vp, _i64, _vp]
     _lib = lib
@@ -445,6 +447,14 @@ def sp_debug_inject(code):
 def sp_debug_tune(kernel, stages=0, blocks_per_sm=0, threads=0, chunks=0):
     _check(load().sp_debug_tune(int(kernel), int(stages), int(blocks_per_sm), int(threads),
                                 int(chunks)))
+
+
+def sp_debug_last_shape(kernel):
+    """Launch shape of this thread's last forward (0) or backward (1) call:
+    dict(threads, chunks, stages, grid, cluster, smem)."""
+    out = (ctypes.c_int32 * 6)()
+    _check(load().sp_debug_last_shape(int(kernel), ctypes.cast(out, _vp)))
+    return dict(zip(("threads", "chunks", "stages", "grid", "cluster", "smem"), list(out)))
 
 
 def sp_debug_philox(ctr_key):

@@ -20,6 +20,8 @@ std::atomic<int> g_inject{SP_OK};
 // Launch-shape overrides for tuning sweeps: [kernel][stages, blocks per SM,
 // threads, chunks per row (backward only)]; 0 = the default rule.
 std::atomic<int> g_tune[2][4] = {{{0}, {0}, {0}, {0}}, {{0}, {0}, {0}, {0}}};
+// The launch shape of this thread's last forward (0) and backward (1) call.
+thread_local LaunchShape g_last_shape[2] = {};
 
 sp_status_t fail(sp_status_t code, const char* fmt, ...) {
   va_list ap;
@@ -244,6 +246,7 @@ LaunchShape pick_shape(int which, int threads, int maxc, int64_t rows, size_t un
   LaunchShape ls{};
   ls.threads = threads;
   ls.maxc = maxc;
+  ls.cluster = 1;
   int stages = g_tune[which][0].load();
   int bps = g_tune[which][1].load();
   if (stages == 0) stages = want_stages;
@@ -341,14 +344,52 @@ void bwd_threads(int64_t h, bool regen, int* threads, int* maxc) {
 // channels, and the block adds one copy-producer warp; one pipeline stage
 // holds the chunk of the t partials and the residual, and the row's Z waits
 // in shared memory for the statistics.
+//
+// Tuning option (sp_debug_tune, forward `chunks` = 2): each row split over a
+// cluster of two CTAs, each handling h / 2 channels; the grid is then as many
+// clusters as the occupancy calculator says can be resident at once.
 LaunchShape fwd_shape_uncached(int64_t rows, int64_t h, int t) {
-  const int threads = fwd_threads(h);
-  const int64_t nchunk = (h + 8 * threads - 1) / (8 * threads);
+  int pair = (g_tune[0][3].load() == 2 && h % 16 == 0) ? 2 : 1;
+  int threads = fwd_threads(h / pair);
+  if (pair > 1 && fwd_kernel_pair(threads, t, 2) == nullptr) {
+    pair = 1;
+    threads = fwd_threads(h);
+  }
+  const int64_t hl = h / pair;
+  const int64_t nchunk = (hl + 8 * threads - 1) / (8 * threads);
   const size_t stage = static_cast<size_t>(t + 1) * threads * 16;
   const size_t fixed = static_cast<size_t>(nchunk) * threads * 16 + 2 * 32 * sizeof(float2);
-  return pick_shape(0, threads + kFwdProducerThreads, static_cast<int>(nchunk), rows, stage,
-                    fixed, kFwdStages, 2, /*stages=*/3, /*blocks per SM=*/512 / threads,
-                    [&](int st) { return fwd_kernel(threads, t, st); });
+  auto kernel_of = [&](int st) {
+    return pair > 1 ? fwd_kernel_pair(threads, t, st) : fwd_kernel(threads, t, st);
+  };
+  LaunchShape ls = pick_shape(0, threads + kFwdProducerThreads, static_cast<int>(nchunk), rows,
+                              stage, fixed, kFwdStages, 2, /*stages=*/3,
+                              /*blocks per SM=*/512 / threads, kernel_of);
+  if (pair > 1) {
+    ls.cluster = pair;
+    int64_t clusters = ls.grid / pair;
+    const void* fn = kernel_of(ls.stages);
+    if (fn != nullptr) {
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = pair;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(pair);
+      cfg.blockDim = dim3(ls.threads);
+      cfg.dynamicSmemBytes = ls.smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) clusters = n;
+      cudaGetLastError();
+    }
+    if (clusters > rows) clusters = rows;
+    if (clusters < 1) clusters = 1;
+    ls.grid = static_cast<int>(clusters * pair);
+  }
+  return ls;
 }
 
 // The shard-input variant of the forward: two streams per stage.
@@ -443,7 +484,23 @@ cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStre
   cudaError_t e = ensure_smem_attr(fn, ls.smem);
   if (e != cudaSuccess) return e;
   void* args[] = {params};
-  e = cudaLaunchKernel(fn, dim3(ls.grid), dim3(ls.threads), args, ls.smem, st);
+  if (ls.cluster > 1) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ls.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ls.grid);
+    cfg.blockDim = dim3(ls.threads);
+    cfg.dynamicSmemBytes = ls.smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+  } else {
+    e = cudaLaunchKernel(fn, dim3(ls.grid), dim3(ls.threads), args, ls.smem, st);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -569,8 +626,11 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   P.withhold = withhold ? 1 : 0;
 
   const LaunchShape ls = fwd_shape(rows, h, t);
-  const cudaError_t e = launch(fwd_kernel(ls.threads - kFwdProducerThreads, t, ls.stages), ls, &P,
-                               static_cast<cudaStream_t>(stream));
+  g_last_shape[0] = ls;
+  const int threads = ls.threads - kFwdProducerThreads;
+  const cudaError_t e = launch(ls.cluster > 1 ? fwd_kernel_pair(threads, t, ls.stages)
+                                              : fwd_kernel(threads, t, ls.stages),
+                               ls, &P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_fwd launch");
   return SP_OK;
 }
@@ -787,6 +847,7 @@ static sp_status_t norm_bwd_common(
 
   const bool has_skip = dz_skip != nullptr;
   const LaunchShape ls = bwd_shape(rows, h, has_skip, regen);
+  g_last_shape[1] = ls;
   const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SP_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need,
@@ -908,6 +969,7 @@ sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
     return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
   const bool has_skip = dz_skip != nullptr;
   const LaunchShape ls = rs_bwd_shape(rows, h, t, has_skip);
+  g_last_shape[1] = ls;
   const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SP_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need,
@@ -1021,6 +1083,19 @@ sp_status_t sp_debug_tune(int32_t kernel, int32_t stages, int32_t blocks_per_sm,
   g_tune[kernel][2].store(threads);
   g_tune[kernel][3].store(chunks);
   g_tune_epoch.fetch_add(1);   // cached launch shapes are stale now
+  return SP_OK;
+}
+
+sp_status_t sp_debug_last_shape(int32_t kernel, int32_t* out) {
+  if ((kernel != 0 && kernel != 1) || out == nullptr)
+    return fail(SP_ERR_INVALID_ARG, "sp_debug_last_shape: bad arguments");
+  const LaunchShape& ls = g_last_shape[kernel];
+  out[0] = kernel == 0 && ls.threads > 0 ? ls.threads - kFwdProducerThreads : ls.threads;
+  out[1] = ls.maxc;
+  out[2] = ls.stages;
+  out[3] = ls.grid;
+  out[4] = ls.cluster;
+  out[5] = static_cast<int32_t>(ls.smem);
   return SP_OK;
 }
 

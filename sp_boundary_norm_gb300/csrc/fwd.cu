@@ -31,15 +31,20 @@
 // The chunk loop is not unrolled (the Philox rounds make its body long): Z of
 // the row waits for the statistics in the thread's own shared-memory slots
 // rather than in registers.
+//
+// A tuning option (not the default: measured slower on GB300) splits every
+// row over a thread-block cluster of two CTAs, each staging and computing
+// h / 2 channels; the halves of the row sums meet through distributed shared
+// memory (fwd_kernel_pair).
 #include "fwd_kernel.cuh"
 
 namespace spb {
 
-template <int NTHR, int TT>
+template <int NTHR, int TT, int CL = 1>
 static const void* fwd_kernel_s(int stages) {
   switch (stages) {
-    case 2: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 2, TT, false>);
-    case 3: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 3, TT, false>);
+    case 2: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 2, TT, false, CL>);
+    case 3: return reinterpret_cast<const void*>(rs_norm_fwd_kernel<NTHR, 3, TT, false, CL>);
     default: return nullptr;
   }
 }
@@ -53,6 +58,17 @@ const void* fwd_kernel(int threads, int t, int stages) {
     case 128: return t8 ? fwd_kernel_s<128, 8>(stages) : fwd_kernel_s<128, 0>(stages);
     case 160: return t8 ? fwd_kernel_s<160, 8>(stages) : fwd_kernel_s<160, 0>(stages);
     case 256: return t8 ? fwd_kernel_s<256, 8>(stages) : fwd_kernel_s<256, 0>(stages);
+    default: return nullptr;
+  }
+}
+
+// Rows split over clusters of two CTAs (the distributed-shared-memory
+// exchange of the row sums): 128 or 256 threads per CTA.
+const void* fwd_kernel_pair(int threads, int t, int stages) {
+  const bool t8 = (t == 8);
+  switch (threads) {
+    case 128: return t8 ? fwd_kernel_s<128, 8, 2>(stages) : fwd_kernel_s<128, 0, 2>(stages);
+    case 256: return t8 ? fwd_kernel_s<256, 8, 2>(stages) : fwd_kernel_s<256, 0, 2>(stages);
     default: return nullptr;
   }
 }

@@ -14,19 +14,31 @@ namespace spb {
 // of each shard in its own buffer; P.partials / P.gathered hold per-shard
 // pointers).  Dropout draws use the token's index in the full sequence in
 // both cases.
-template <int NTHR, int STAGES, int TT, bool SHARD>
+// CL = 2: the kernel runs in clusters of two CTAs that split every token row
+// in halves of h / 2 channels (h a multiple of 16); each CTA reduces its half
+// of the row sums, the two exchange them through distributed shared memory
+// (one mbarrier hand-off per reduction, bounded waits) and both add them in
+// the same order (CTA 0's part first), so both normalise with the same
+// statistics.  Launched with a cluster dimension of 2; CTA 0 stores mean and
+// rstd.
+template <int NTHR, int STAGES, int TT, bool SHARD, int CL = 1>
 __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     rs_norm_fwd_kernel(const FwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
+  __shared__ __align__(8) uint64_t xbar[2];   // CL > 1: the partner's row sums arrived
+  __shared__ __align__(8) float2 xpub[2];     // CL > 1: this CTA's row sums, published
   constexpr int kWarps = NTHR / 32;   // compute warps; warp kWarps issues the copies
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   // input streams summed per element (compile-time when specialised)
   const int t = SHARD ? 1 : (TT > 0 ? TT : P.map.t);
   const int64_t h = P.map.h;
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+  const int64_t hl = h / CL;          // channels of a row this CTA handles
+  const int64_t coff = crank * hl;    // their first channel
   constexpr int kChunk = 8 * NTHR;
-  const int nchunk = static_cast<int>((h + kChunk - 1) / kChunk);
+  const int nchunk = static_cast<int>((hl + kChunk - 1) / kChunk);
   constexpr int kStream = NTHR * 16;
   const int stage_bytes = (t + 1) * kStream;
   uint8_t* zbuf = smem + STAGES * stage_bytes + tid * 16;   // own slots, stride kStream
@@ -38,23 +50,31 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], kWarps);
     }
+    if (CL > 1) {
+      mbar_init(&xbar[0], 1);
+      mbar_init(&xbar[1], 1);
+    }
     mbar_fence_init();
   }
-  __syncthreads();
+  if (CL > 1)
+    cluster_sync_all();   // the partner's mbarriers are initialised too
+  else
+    __syncthreads();
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
-  // this block's rows: every G-th token from blockIdx.x when blocks get many
-  // rows (neighbouring tokens are then in flight together), else a
-  // contiguous range
-  const int64_t G = gridDim.x;
+  // this block's rows (a cluster's: both CTAs walk the same rows): every G-th
+  // token when blocks get many rows (neighbouring tokens are then in flight
+  // together), else a contiguous range
+  const int64_t G = gridDim.x / CL;
+  const int64_t bid = blockIdx.x / CL;
   const bool strided = P.rows >= 32 * G;
   const int64_t step = strided ? G : 1;
   int64_t r0, nrows;
   if (strided) {
-    r0 = blockIdx.x;
+    r0 = bid;
     nrows = (P.rows - 1 - r0) / G + 1;
   } else {
-    block_rows(P.rows, blockIdx.x, G, &r0, &nrows);
+    block_rows(P.rows, bid, G, &r0, &nrows);
   }
   const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
 
@@ -73,7 +93,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     int64_t item = 0;
     for (int64_t ri = 0; ri < nrows; ++ri) {
       if (ri > 0) pf.next(P.map, step);
-      const int64_t goff = pf.row * h, roff = pf.local * h;
+      const int64_t goff = pf.row * h + coff, roff = pf.local * h + coff;
       const int kk = pf.k;
       for (int ch = 0; ch < nchunk; ++ch, ++item) {
         const int s = static_cast<int>(item % STAGES);
@@ -84,7 +104,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
         const bool withheld = P.withhold != 0 && blockIdx.x == 0 && item == 0;   // test hook
         if (lane == 0 && !withheld) {
           const int cc = ch * kChunk;
-          const int n = (h - cc < kChunk) ? static_cast<int>(h - cc) : kChunk;
+          const int n = (hl - cc < kChunk) ? static_cast<int>(hl - cc) : kChunk;
           const uint32_t bytes = static_cast<uint32_t>(n) * 2u;
           uint8_t* dst = smem + s * stage_bytes;
           mbar_arrive_expect_tx(&bar_full[s], bytes * static_cast<uint32_t>(t + 1));
@@ -107,6 +127,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       if (!mbar_wait(&bar_full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1)))
         timed_out = true;
     if (timed_out && P.status != nullptr) *P.status = SP_ERR_TIMEOUT;
+    if (CL > 1) cluster_sync_all();
     return;
   }
 
@@ -114,14 +135,44 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
   cur.init(P.map, r0);
   int slot_sel = 0;
   const float inv_h = 1.f / static_cast<float>(h);
+
+  // CL > 1: adds the partner CTA's part of a row sum to this CTA's part, in
+  // CTA order.  Exchange xi uses slot xi & 1 and that slot's phase parity
+  // (xi >> 1) & 1; a slot is reused two exchanges later, which the partner
+  // can reach only after this CTA's next exchange, i.e. after every warp here
+  // has read the slot.
+  uint32_t xi = 0;
+  auto pair_sum = [&](float2 part) -> float2 {
+    if constexpr (CL == 1) {
+      return part;
+    } else {
+      const uint32_t peer = crank ^ 1u;
+      const int slot = static_cast<int>(xi & 1u);
+      const uint32_t par = (xi >> 1) & 1u;
+      ++xi;
+      if (tid == 0) {
+        xpub[slot] = part;
+        mbar_arrive_remote(cluster_map(&xbar[slot], peer));
+      }
+      float2 other = make_float2(0.f, 0.f);
+      if (lane == 0) {
+        if (!timed_out && !mbar_wait_cluster(&xbar[slot], par)) timed_out = true;
+        if (!timed_out) other = ld_cluster_f2(cluster_map(&xpub[slot], peer));
+      }
+      other.x = __shfl_sync(0xFFFFFFFFu, other.x, 0);
+      other.y = __shfl_sync(0xFFFFFFFFu, other.y, 0);
+      return crank == 0 ? make_float2(part.x + other.x, part.y + other.y)
+                        : make_float2(other.x + part.x, other.y + part.y);
+    }
+  };
   for (int64_t ri = 0; ri < nrows; ++ri) {
     if (ri > 0) cur.next(P.map, step);
     const int64_t row = cur.row;
     const int k = cur.k;
     const int64_t local = cur.local;
-    uint16_t* zrow = P.z[k] + local * h + c0;
-    uint8_t* mrow = P.mask[k] + local * h + c0;
-    const uint64_t e_row = static_cast<uint64_t>(row * h + c0);   // global element index
+    uint16_t* zrow = P.z[k] + local * h + coff + c0;
+    uint8_t* mrow = P.mask[k] + local * h + coff + c0;
+    const uint64_t e_row = static_cast<uint64_t>(row * h + coff + c0);   // global element index
 
     // ---- pass 1: g* sum, bias, dropout, residual -> Z (stored) ----------
     float lsum = 0.f, lsq = 0.f;
@@ -136,7 +187,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
       float y[8];
       uint4 rv = make_uint4(0, 0, 0, 0);
-      if (cc + c0 < h) {
+      if (cc + c0 < hl) {
         const uint8_t* slot = smem + stage * stage_bytes + tid * 16;
         unpack8(lds16(slot), y);
         if (!SHARD) {
@@ -148,8 +199,8 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_empty[stage]);   // the stage is free again
-      if (cc + c0 < h) {
-        const uint4 bv = ldg16(P.bias + cc + c0);
+      if (cc + c0 < hl) {
+        const uint4 bv = ldg16(P.bias + coff + cc + c0);
         add8_bf16(bv, y);   // + bias
         // dropout: element e keeps iff its Philox word >= thr
         uint2 keep = make_uint2(0x01010101u, 0x01010101u);
@@ -204,7 +255,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     // in a second pass as the mean of (Z - mean)^2.
     float mean = 0.f, rstd;
     if (is_ln) {
-      const float2 sums = warps_sum2<kWarps>(lsum, lsq, red + 32 * slot_sel);
+      const float2 sums = pair_sum(warps_sum2<kWarps>(lsum, lsq, red + 32 * slot_sel));
       slot_sel ^= 1;
       mean = sums.x * inv_h;
       const float var1 = sums.y * inv_h - mean * mean;
@@ -215,38 +266,43 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
         const float nmean = -mean;
 #pragma unroll 1
         for (int ch = 0; ch < nchunk; ++ch) {
-          if (ch * kChunk + c0 < h) {
+          if (ch * kChunk + c0 < hl) {
             float d[8];
             add8_bf16_bcast(lds16(zbuf + ch * kStream), nmean, d);   // z - mean
 #pragma unroll
             for (int e = 0; e < 8; e += 2) fma2(lsqa, lsqb, d[e], d[e + 1], d[e], d[e + 1]);
           }
         }
-        const float var = warps_sum<kWarps>(lsqa + lsqb, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
+        const float var =
+            pair_sum(make_float2(warps_sum<kWarps>(lsqa + lsqb,
+                                                   reinterpret_cast<float*>(red + 32 * slot_sel)),
+                                 0.f)).x * inv_h;
         slot_sel ^= 1;
         rstd = rsqrtf(var + P.eps);
       }
     } else {
-      const float ms = warps_sum<kWarps>(lsq, reinterpret_cast<float*>(red + 32 * slot_sel)) * inv_h;
+      const float ms =
+          pair_sum(make_float2(warps_sum<kWarps>(lsq, reinterpret_cast<float*>(red + 32 * slot_sel)),
+                               0.f)).x * inv_h;
       slot_sel ^= 1;
       rstd = rsqrtf(ms + P.eps);
     }
 
     // ---- normalise and write into the all-gather destination(s) ----------
-    const int64_t orow = row * h + c0;
-    uint16_t* g0_row = SHARD ? P.gathered[k] + local * h + c0
+    const int64_t orow = row * h + coff + c0;
+    uint16_t* g0_row = SHARD ? P.gathered[k] + local * h + coff + c0
                              : (P.n_gather > 0 ? P.gathered[0] + orow : nullptr);
 #pragma unroll 1
     for (int ch = 0; ch < nchunk; ++ch) {
       const int cc = ch * kChunk;
-      if (cc + c0 < h) {
+      if (cc + c0 < hl) {
         const uint4 zv = lds16(zbuf + ch * kStream);
-        const uint4 gv = ldg16(P.gamma + cc + c0);
+        const uint4 gv = ldg16(P.gamma + coff + cc + c0);
         float o[8];
         if (is_ln) {
           float g[8], bt[8];
           unpack8(gv, g);
-          unpack8(ldg16(P.beta + cc + c0), bt);
+          unpack8(ldg16(P.beta + coff + cc + c0), bt);
           add8_bf16_bcast(zv, -mean, o);   // z - mean
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
@@ -266,12 +322,13 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
           for (int j = 1; j < P.n_gather; ++j) st16_stream(P.gathered[j] + orow + cc, ob);
       }
     }
-    if (tid == 0) {
+    if (tid == 0 && crank == 0) {
       if (is_ln) P.mean[k][local] = mean;
       P.rstd[k][local] = rstd;
     }
   }
   if (timed_out && P.status != nullptr) *P.status = SP_ERR_TIMEOUT;
+  if (CL > 1) cluster_sync_all();   // no partner reads this CTA's shared memory any more
 }
 
 }  // namespace spb

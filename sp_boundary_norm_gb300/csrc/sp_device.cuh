@@ -323,6 +323,64 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
       : "memory");
 }
 
+// ------------------------------------------------------------ clusters --
+// A token row split over the CTAs of a thread-block cluster: each CTA
+// publishes its part of the row sums in its own shared memory and arrives on
+// the partner's mbarrier (release, cluster scope); the partner waits on its
+// own mbarrier (acquire, cluster scope, bounded) and reads the value through
+// distributed shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits (a CTA may not
+// exit while a partner can still reach its shared memory).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address, in the cluster's shared window, of variable p of CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity) {
+  if (mbar_try_wait_cluster(b, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_cluster(b, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t cluster_addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y)
+               : "r"(cluster_addr) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------ tensor memory --
 // Tensor memory (TMEM, 128 lanes x 512 columns of 32 bits per SM) used as
 // per-thread accumulator storage: warp w reaches lanes 32*(w % 4) .. +31, one

@@ -135,6 +135,7 @@ struct LaunchShape {
   int grid;        // blocks
   size_t smem;     // dynamic shared memory bytes
   bool fits;       // false: no instantiated shape fits this SM's shared memory
+  int cluster;     // CTAs per thread-block cluster (forward: CTAs sharing a row); 1 = none
 };
 
 int device_sm_count();
@@ -146,6 +147,8 @@ sp_status_t record_error(sp_status_t code, const char* message);
 // Forward: (threads, ranks t, pipeline stages); backward: (threads, chunks per
 // row, ring rows).
 const void* fwd_kernel(int threads, int t, int stages);
+// The forward with each row split over a cluster of two CTAs (threads 128 or 256).
+const void* fwd_kernel_pair(int threads, int t, int stages);
 const void* fwd_shard_kernel(int threads, int stages);
 const void* bwd_kernel(int threads, int maxc, int ring);
 const void* bwd_regen_kernel(int threads, int maxc, int ring);

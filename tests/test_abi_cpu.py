@@ -132,6 +132,21 @@ def test_injected_failure_is_returned_once(lib):
     assert lib.sp_allgather_seq(arr, 1, 8, 64, 0, None, 0, arr, 1, None, None) == 1
 
 
+def test_last_shape_hook_host_rules(lib):
+    """The shape hook is per thread: zeros before a thread's first call; bad
+    kernel indices are rejected."""
+    import threading
+    from sp_boundary_norm_gb300 import binding
+    binding.load()
+    got = {}
+    th = threading.Thread(target=lambda: got.update(binding.sp_debug_last_shape(0)))
+    th.start()
+    th.join()
+    assert got == dict(threads=0, chunks=0, stages=0, grid=0, cluster=0, smem=0)
+    with pytest.raises(binding.SpError):
+        binding.sp_debug_last_shape(2)
+
+
 def test_workspace_size_shape_rules(lib):
     from sp_boundary_norm_gb300 import binding
     binding.load()

@@ -85,11 +85,27 @@ def test_forward_equals_unsharded_path_sliced_by_token(variant):
     assert not bad.any(), f"{bad.sum()} elements off"
 
 
-def test_layernorm_rows_with_large_mean():
+@pytest.fixture
+def fwd_split():
+    """Split every forward row over a thread-block cluster of `split` CTAs
+    (forcing the threads per CTA if given) for one test; the automatic choice
+    is restored afterwards."""
+    def force(split, threads=0):
+        C.sp.sp_debug_tune(0, 0, 0, threads, split)
+    yield force
+    C.sp.sp_debug_tune(0, 0, 0, 0, 0)
+
+
+@pytest.mark.parametrize("split", [1, 2])
+def test_layernorm_rows_with_large_mean(fwd_split, split):
     """The forward takes the LayerNorm variance as E[Z^2] - mean^2 only where
     mean^2 <= var / 4 and recomputes it from (Z - mean)^2 elsewhere.  Residual
     rows shifted by 0 to 300 standard deviations (either sign, several near the
-    switch at 0.5) put tokens on both sides; all must meet the tolerances."""
+    switch at 0.5) put tokens on both sides; all must meet the tolerances.
+    With split = 2 each row is split over a CTA pair, so the recomputation
+    takes a second exchange of row sums between the two CTAs."""
+    if split == 2:
+        fwd_split(2, 128)
     w = wl.Workload("lm", t=4, b=1, s=288, h=1024, draw_seed=97)
     inp = wl.forward_inputs(w, C.DEV)
     shifts = [0.0, 0.25, 0.45, 0.49, 0.5, 0.51, 0.55, 0.7, 1.0, 3.0, 30.0, 300.0, -0.5, -40.0]
@@ -105,6 +121,64 @@ def test_layernorm_rows_with_large_mean():
     ratio = np.concatenate([m * m / (1.0 / (r * r) - w.eps) for m, r in
                             zip(ref["mean"], ref["rstd"])], axis=1)
     assert (ratio < 0.2).any() and (ratio > 0.3).any() and (ratio > 1e3).any()
+    assert C.sp.sp_debug_last_shape(0)["cluster"] == split
+
+
+@pytest.mark.parametrize("variant,threads", [
+    (dict(), 128),
+    (dict(norm="rmsnorm", eps=1e-6), 128),
+    (dict(t=3, s=48), 128),
+    (dict(b=3, s=40, t=4), 128),
+    (dict(h=16, s=16), 128),
+    (dict(h=528, s=32), 128),
+    (dict(p=0.0), 128),
+    (dict(n_gather=2), 128),
+    (dict(seed=2**40 + 17, offset=2**33 + 5), 128),
+    (dict(h=4096, s=64, t=8), 0),
+    (dict(h=8192, s=64, t=8), 0),
+    (dict(h=8192, s=16, t=8), 256),
+    (dict(h=16384, s=8), 0),
+])
+def test_forward_row_split_over_a_cta_pair(fwd_split, variant, threads):
+    """The forward with every token row split over a thread-block cluster of
+    two CTAs (h / 2 channels each, the row sums exchanged through distributed
+    shared memory): Z and the mask bit for bit, the statistics and O within
+    the tolerances, against the oracle."""
+    fwd_split(2, threads)
+    w = wl.Workload("cp", t=2, b=1, s=64, h=512, draw_seed=141).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    shape = C.sp.sp_debug_last_shape(0)
+    assert shape["cluster"] == 2 and shape["grid"] % 2 == 0, shape
+    _full_fwd_compare(w, inp, out)
+
+
+def test_forward_row_split_ragged_and_70b_sampled(fwd_split):
+    """The CTA-pair forward on packed uneven shards (full compare) and on the
+    70B shape (sampled rows and the drop rate)."""
+    fwd_split(2, 128)
+    lengths = (33, 64, 7, 1, 90, 12)
+    w = wl.Workload("rp", t=5, b=1, s=sum(lengths), h=512, seqlens=lengths, draw_seed=142)
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    assert C.sp.sp_debug_last_shape(0)["cluster"] == 2
+    _full_fwd_compare(w, inp, out)
+    del inp, out
+    fwd_split(2)
+    w = wl.WORKLOADS["70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    assert C.sp.sp_debug_last_shape(0)["cluster"] == 2
+    C.check_fwd_rows(w, inp, out, C.sample_tokens(w, 64))
+    kept = sum(int(m.sum()) for m in out["mask"])
+    n = w.tokens * w.h
+    assert abs((1 - kept / n) - w.p) < 5 * np.sqrt(w.p * (1 - w.p) / n)
 
 
 @pytest.mark.parametrize("variant", [
