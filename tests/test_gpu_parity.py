@@ -630,6 +630,8 @@ def test_backward_tensor_memory_shapes(bwd_shape, shape, h):
     bwd_shape(*shape)
     w = wl.Workload("tm", t=2, b=1, s=1216, h=h, draw_seed=101)
     inp, fwd, b, out = _bwd_setup(w)
+    got = C.sp.sp_debug_last_shape(1)
+    assert (got["threads"], got["chunks"]) == shape, got
     C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], None, out, C.sample_tokens(w, 96))
     C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
 
@@ -642,6 +644,8 @@ def test_backward_tensor_memory_variants(bwd_shape, variant):
     skip = v.pop("skip", False)
     w = wl.Workload("tv", t=2, b=1, s=640, h=8192, draw_seed=102).with_(**v)
     inp, fwd, b, out = _bwd_setup(w, skip, n_gather=w.n_gather)
+    got = C.sp.sp_debug_last_shape(1)
+    assert (got["threads"], got["chunks"]) == (256, 4), got
     C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out, C.sample_tokens(w, 64))
     C.check_param_grads(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out)
 
@@ -658,6 +662,8 @@ def test_backward_tensor_memory_mask_free_and_deterministic(bwd_shape):
                             dbeta=got["dbeta"], dbias=got["dbias"], workspace=got["ws"])
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
+    shape = C.sp.sp_debug_last_shape(1)
+    assert (shape["threads"], shape["chunks"]) == (256, 4), shape
     for other in (again, got):
         for a, c in zip(first["dres"] + first["dgat"], other["dres"] + other["dgat"]):
             assert torch.equal(a, c)
@@ -869,3 +875,19 @@ def test_one_kernel_across_shared_memory_sizes():
         out = C.run_fwd(w, inp)
         torch.cuda.synchronize()
         C.check_fwd_rows(w, inp, out, C.sample_tokens(w, 8))
+
+
+# ------------------------------------------------------ default launch shapes
+
+@pytest.mark.parametrize("h,fwd_threads,bwd_shape", [(8192, 256, (512, 2)), (5120, 128, (320, 2)),
+                                                     (4096, 256, (256, 2))])
+def test_default_launch_shapes(h, fwd_threads, bwd_shape):
+    """The launch shapes the library picks by default for the workloads'
+    row widths (the measured choices): forward threads per block (whole rows,
+    no cluster), backward (threads, chunks per row)."""
+    w = wl.Workload("ds", t=8, b=1, s=64, h=h, draw_seed=151)
+    _bwd_setup(w)
+    f = C.sp.sp_debug_last_shape(0)
+    assert f["threads"] == fwd_threads and f["cluster"] == 1, f
+    b = C.sp.sp_debug_last_shape(1)
+    assert (b["threads"], b["chunks"]) == bwd_shape, b
