@@ -6,8 +6,14 @@ and the backward (norm / dropout backward, all-gather of the partials'
 gradient, parameter gradients), on the 70B-shape workload (t = 8 emulated
 ranks, b = 1, s = 16384, h = 8192, bf16).
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-instead, on bounded samples of the same workload.
+Prints one JSON line (rank 0).  ``value`` times K whole steps (replayed as
+CUDA graphs of up to 8 steps) between two CUDA events on the launching
+stream, inputs resident in HBM (larger than L2); the forward / backward split
+comes from a second loop with one graph per call, and the roofline of the
+dominant kernel (the forward) from its per-launch duration in a third loop
+of graphs of 8 back-to-back calls.  ``e2e`` repeats the step through the
+public API with pinned host buffers copied in and out.  ``--impl reference``
+times the CPU oracle instead, on bounded samples of the same workload.
 
 Launch: ``python bench.py [--gpus N] [--steps K] [--warmup W]``; for N > 1
 under torch.distributed.run, each rank processes its own batch (weak
