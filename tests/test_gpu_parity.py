@@ -592,6 +592,45 @@ def test_unfused_pipeline_matches_oracle(variant):
     assert got.shape == compare.bf16_bits(full).shape
 
 
+def test_unfused_pipeline_70b_sampled():
+    """The unfused boundary (bench --pipeline unfused) at the 70B shape in the
+    bench's launch configuration, on sampled tokens: the reduce-scatter's bf16
+    shard rows equal the oracle's rank-ascending float32 sum rounded to bf16,
+    and the shard step's Z and mask (bit for bit), statistics and O (within
+    the tolerances) equal the oracle's token-wise forward of those rows."""
+    from oracle import bf16 as obf
+    from oracle import collectives as oc
+    w = wl.WORKLOADS["70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    y, o, out = _run_unfused(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    tokens = C.sample_tokens(w, 48)
+    toks = torch.from_numpy(tokens).to(C.DEV)
+    prow = [C.f32(P.reshape(-1, w.h).index_select(0, toks))[None] for P in inp["partials"]]
+    y16 = obf.bf16_round(np.concatenate(oc.reduce_scatter_seq(prow)[0], axis=1)[0])
+    locs = [C.token_shard(w, g) for g in tokens]
+    row = lambda lst, k, l: lst[k].reshape(-1, w.h)[l]
+    got_y = np.stack([compare.bf16_bits(row(y, k, l)) for k, l in locs])
+    assert np.array_equal(got_y, compare.bf16_bits(y16)), "reduce-scatter rows"
+    rrow = np.stack([C.f32(row(inp["residual"], k, l)) for k, l in locs])
+    ref = ob.forward_rows(y16[None], rrow, tokens, C.f32(inp["bias"]), C.f32(inp["gamma"]),
+                          C.f32(inp["beta"]), eps=w.eps, p=w.p, seed=w.seed, offset=w.offset,
+                          norm=w.norm)
+    z = np.stack([compare.bf16_bits(row(out["z"], k, l)) for k, l in locs])
+    assert np.array_equal(z, compare.bf16_bits(ref["z"])), "Z"
+    m = np.stack([row(out["mask"], k, l).cpu().numpy() for k, l in locs])
+    assert np.array_equal(m, ref["mask"]), "mask"
+    rs = np.array([float(out["rstd"][k].reshape(-1)[l]) for k, l in locs])
+    assert not compare.f32_rel_mismatch(rs, ref["rstd"]).any(), "rstd"
+    mu = np.array([float(out["mean"][k].reshape(-1)[l]) for k, l in locs])
+    assert not compare.f32_rel_mismatch(mu, ref["mean"]).any(), "mean"
+    got_o = np.stack([compare.bf16_bits(row(o, k, l)) for k, l in locs])
+    assert not compare.bf16_mismatch(got_o, ref["out_exact"], ref["out_magnitude"]).any(), "O"
+    g = compare.bf16_bits(out["gathered"][0].reshape(-1, w.h).index_select(0, toks))
+    assert np.array_equal(g, got_o), "gathered rows are the shards' O"
+
+
 def test_unfused_mask_equals_fused_mask():
     w = wl.Workload("ufm", t=4, b=1, s=128, h=1024, draw_seed=62)
     inp = wl.forward_inputs(w, C.DEV)
