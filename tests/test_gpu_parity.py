@@ -219,10 +219,16 @@ def test_forward_gathered_copies_identical_and_layout():
         assert torch.equal(g.view(torch.int16), g0.view(torch.int16))
 
 
-@pytest.mark.parametrize("lengths,t", [((5, 17, 3, 40), 8), ((3,), 8), ((100, 1, 1), 3),
-                                       ((33, 64, 7, 1, 90, 12), 5)])
-def test_forward_ragged_packed_full_compare(lengths, t):
-    w = wl.Workload("r", t=t, b=1, s=sum(lengths), h=512, seqlens=tuple(lengths), draw_seed=23)
+@pytest.mark.parametrize("lengths,t,extra", [((5, 17, 3, 40), 8, {}), ((3,), 8, {}),
+                                             ((100, 1, 1), 3, {}),
+                                             ((33, 64, 7, 1, 90, 12), 5, {}),
+                                             ((33, 64, 7, 1, 90, 12), 5,
+                                              dict(norm="rmsnorm", eps=1e-6)),
+                                             ((5, 17, 3, 40), 8, dict(n_gather=3)),
+                                             ((50, 13, 9), 8, dict(h=5120))])
+def test_forward_ragged_packed_full_compare(lengths, t, extra):
+    w = wl.Workload("r", t=t, b=1, s=sum(lengths), h=512, seqlens=tuple(lengths),
+                    draw_seed=23).with_(**extra)
     inp = wl.forward_inputs(w, C.DEV)
     out = C.run_fwd(w, inp)
     torch.cuda.synchronize()
@@ -415,12 +421,25 @@ def test_backward_full_compare(variant, with_skip):
     C.check_param_grads(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out)
 
 
-def test_backward_ragged_packed():
+@pytest.mark.parametrize("variant", [
+    dict(),
+    dict(norm="rmsnorm", eps=1e-6),
+    dict(skip=True),
+    dict(n_gather=2),
+    dict(h=5120, t=8),
+])
+def test_backward_ragged_packed(variant):
+    """Packed uneven shards through the backward, every token compared, with
+    RMSNorm, the skip-path gradient, two gathered copies and the h = 5120
+    tensor-memory shape."""
+    v = dict(variant)
+    skip = v.pop("skip", False)
     lengths = (5, 17, 3, 40, 1, 9)
-    w = wl.Workload("rb", t=4, b=1, s=sum(lengths), h=256, seqlens=lengths, draw_seed=32)
-    inp, fwd, b, out = _bwd_setup(w)
-    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], None, out, np.arange(w.tokens))
-    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], None, out)
+    w = wl.Workload("rb", t=4, b=1, s=sum(lengths), h=256, seqlens=lengths,
+                    draw_seed=32).with_(**v)
+    inp, fwd, b, out = _bwd_setup(w, skip, n_gather=w.n_gather)
+    C.check_bwd_rows(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out, np.arange(w.tokens))
+    C.check_param_grads(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], out)
 
 
 @pytest.mark.parametrize("name", ["bwd70b", "bwd70b_rms"])
