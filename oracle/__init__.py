@@ -36,6 +36,12 @@ Modules and what pins each one (tests under ``tests/test_oracle_*.py``):
   transpose identity <AG x, y> = <x, RS y>.
 * ``accounting``  -- the block shape trace and the activation-memory law.
   Pinned by the printed numbers of L7 (33.6 MB / 4.2 MB; 1.34 GB / 167.8 MB).
+* ``compare``     -- the parity checker's tolerance predicates.  Pinned by
+  cases each predicate must reject (2 ulps either side and across zero, an
+  error above the magnitude floor, 2e-5 on a statistic, a column sum with one
+  term dropped, doubled or negated), by the oracle's magnitudes staying tight
+  enough that the floor rarely exceeds one ulp, and by a float32 LayerNorm
+  passing the bar with few elements accepted through the floor alone.
 
 Parity unpinned: none of the functions above.  (Throughput has no page
 figure to pin against; it is measured, not compared.)

@@ -36,14 +36,40 @@ def bf16_bits(x):
     return (a.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
-def bf16_mismatch(gpu_bits, ref_exact, magnitude, max_ulp=1):
-    """Boolean mask of elements failing the bf16 tolerance."""
+def _bf16_tests(gpu_bits, ref_exact, magnitude, max_ulp):
+    """(within max_ulp of the rounded exact value, within the magnitude floor)."""
     ref_bits = bf16_bits(bf16_round(ref_exact))
     ulps = np.abs(order_key(gpu_bits) - order_key(ref_bits))
     gpu = (np.asarray(gpu_bits).astype(np.uint32) << np.uint32(16)).view(np.float32)
     abs_err = np.abs(gpu.astype(np.float64) - np.asarray(ref_exact, dtype=np.float64))
-    ok = (ulps <= max_ulp) | (abs_err <= FLOOR_REL * np.asarray(magnitude, dtype=np.float64))
-    return ~ok
+    return ulps <= max_ulp, abs_err <= FLOOR_REL * np.asarray(magnitude, dtype=np.float64)
+
+
+def bf16_mismatch(gpu_bits, ref_exact, magnitude, max_ulp=1):
+    """Boolean mask of elements failing the bf16 tolerance."""
+    near, floor = _bf16_tests(gpu_bits, ref_exact, magnitude, max_ulp)
+    return ~(near | floor)
+
+
+def bf16_floor_only(gpu_bits, ref_exact, magnitude, max_ulp=1):
+    """Boolean mask of elements that pass the bf16 tolerance only through the
+    magnitude floor (more than max_ulp from the rounded exact value, but
+    within 2**-16 of the expression's terms): the cancelled results the floor
+    exists for.  Tests bound how many there are, so that the floor cannot
+    quietly stand in for the 1-ulp bar."""
+    near, floor = _bf16_tests(gpu_bits, ref_exact, magnitude, max_ulp)
+    return ~near & floor
+
+
+def floor_only_bound(n):
+    """Most elements out of n that may pass only through the magnitude floor.
+
+    A float32 evaluation misses the 1-ulp bar only where its result cancels
+    to below about 2**-15 of the expression's terms; with the workloads'
+    distributions that is a few elements in ten million (a float32 emulation
+    of the LayerNorm output on the s = h = 4096 inputs: 2 of 8,388,608).  The
+    bound allows eight times that rate plus a constant for small tensors."""
+    return 8 + int(2e-6 * n)
 
 
 def f32_rel_mismatch(gpu, ref, tol=1e-5):
