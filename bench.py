@@ -310,6 +310,42 @@ class Step:
                             dbias=self.dbias, workspace=self.ws)
 
 
+    def inputs(self):
+        """The step's inputs, as a caller would copy them in."""
+        return self.inp["partials"] + self.inp["residual"] + self.dy
+
+    def outputs(self):
+        """The step's results, as a caller would copy them out."""
+        return self.gathered + self.dres + self.dgat + [self.dgamma, self.dbeta, self.dbias]
+
+
+class BucketedStep:
+    """One step of a packed batch bucketed by length: the boundary's forward
+    and backward on every bucket in turn (each bucket a packed batch of its
+    own with its cu_seqlens), covering the same sequences as the whole batch."""
+
+    def __init__(self, w, device, buckets, **kw):
+        self.buckets = buckets
+        self.steps = [Step(w.with_(name=f"{w.name}-bucket{i}", s=b.tokens,
+                                   seqlens=tuple(b.lengths), draw_seed=w.draw_seed + 100 + i),
+                           device, **kw) for i, b in enumerate(buckets)]
+        self.sp = self.steps[0].sp
+
+    def fwd(self):
+        for st in self.steps:
+            st.fwd()
+
+    def bwd(self):
+        for st in self.steps:
+            st.bwd()
+
+    def inputs(self):
+        return [x for st in self.steps for x in st.inputs()]
+
+    def outputs(self):
+        return [x for st in self.steps for x in st.outputs()]
+
+
 def capture(fn, device):
     """One call of the step's forward or backward as a CUDA graph.
 
@@ -408,6 +444,26 @@ def time_device(step, steps, warmup, world, device, launch="graph"):
     return total_ms, fwd_ms, bwd_ms, back_to_back, sampler.summary(t0, t1)
 
 
+def time_each_step(step_list, steps, device):
+    """ms per forward + backward of each step, alone: one graph of the pair,
+    replayed `steps` times between two events."""
+    stream = torch.cuda.current_stream(device)
+    out = []
+    for st in step_list:
+        g = capture(lambda: (st.fwd(), st.bwd()), device)
+        for _ in range(3):
+            g()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(stream)
+        for _ in range(steps):
+            g()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        out.append(a.elapsed_time(b) / steps)
+    return out
+
+
 def time_e2e(step_a, step_b, steps, device):
     """The step through the public API with host buffers, end to end (wall
     clock, synchronised at both ends): every step copies its inputs in from
@@ -417,8 +473,8 @@ def time_e2e(step_a, step_b, steps, device):
     of step i+1 and the copy-out of step i on their own streams while step i
     computes."""
     sets = [step_a, step_b]
-    ins = lambda st: st.inp["partials"] + st.inp["residual"] + st.dy
-    outs = lambda st: st.gathered + st.dres + st.dgat + [st.dgamma, st.dbeta, st.dbias]
+    ins = lambda st: st.inputs()
+    outs = lambda st: st.outputs()
     host_in = [x.cpu().pin_memory() for x in ins(step_a)]
     host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs(step_a)]
     h2d = sum(x.numel() * x.element_size() for x in host_in)
@@ -554,7 +610,7 @@ def cpu_baseline(w, seconds=10.0, n_tokens=64):
     cores = max(out)
     value, reps, elapsed = out[cores]
     return {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "single_thread_value": round(out[1][0], 2),
+            "nproc": os.cpu_count(), "single_thread_value": round(out[1][0], 2),
             "sample": f"{reps} steps of {cores} oracle processes (one per host core) x "
                       f"{n_tok} tokens of the {w.name} shape (t={w.t}, h={w.h}), fwd+bwd, "
                       f"{elapsed:.1f} s wall; one process alone: {out[1][0]:.1f} tokens/s"}
@@ -581,8 +637,18 @@ def run_ours(args):
     if args.norm is not None:
         w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
                     name=f"{w.name}-{args.norm}")
-    step = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
-                bwd_entry=args.bwd_entry)
+    kw = dict(n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
+              bwd_entry=args.bwd_entry)
+    buckets = None
+    if args.bucket:
+        if not w.ragged:
+            raise SystemExit("--bucket: packed workloads only (--workload ragged)")
+        from sp_boundary_norm_gb300 import bucketing as bk
+        buckets = bk.bucket_by_tokens(w.seqlens, max_cv=args.max_cv)
+        make_step = lambda: BucketedStep(w, device, buckets, **kw)
+    else:
+        make_step = lambda: Step(w, device, **kw)
+    step = make_step()
     total_ms, fwd_ms, bwd_ms, b2b, clocks = time_device(step, args.steps, args.warmup, world,
                                                         device, args.launch)
     rejected = False
@@ -607,11 +673,30 @@ def run_ours(args):
     step_ms = total_ms / args.steps
     achieved = fb / (b2b["fwd_ms"] / 1e3) / 1e9
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    step_b = Step(w, device, n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
-                  bwd_entry=args.bwd_entry)
+    step_b = make_step()
     e2e_ms, h2d, d2h = time_e2e(step, step_b, e2e_steps, device)
     del step_b
     e2e_ms = max_over_ranks(e2e_ms, world, device)
+    bucketing = None
+    if buckets is not None:
+        # each bucket alone, then the same sequences as one packed batch
+        per = time_each_step(step.steps, args.steps, device)
+        whole = Step(w, device, **kw)
+        w_total, _, _, w_b2b, _ = time_device(whole, args.steps, args.warmup, world, device,
+                                              args.launch)
+        del whole
+        bucketing = {
+            "max_cv": args.max_cv,
+            "buckets": [{"lengths": list(b.lengths), "length_cv": round(b.length_cv, 4),
+                         "tokens": b.tokens, "ms_per_step": round(ms, 4),
+                         "tokens_per_s": round(b.tokens / (ms / 1e3), 1)}
+                        for b, ms in zip(buckets, per)],
+            "unbucketed": {"length_cv": round(bk.length_cv(w.seqlens), 4),
+                           "ms_per_step": round(w_total / args.steps, 4),
+                           "tokens_per_s": round(w.tokens * args.steps / (w_total / 1e3), 1),
+                           "fwd_ms_back_to_back": round(w_b2b["fwd_ms"], 4),
+                           "bwd_ms_back_to_back": round(w_b2b["bwd_ms"], 4)},
+        }
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, seconds=args.cpu_seconds)
@@ -623,7 +708,9 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name}: LayerNorm boundary fwd+bwd, t={w.t} emulated ranks, "
-                               f"b={w.b}, s={w.s}, h={w.h}, p={w.p}, n_gather={args.n_gather}",
+                               f"b={w.b}, s={w.s}, h={w.h}, p={w.p}, n_gather={args.n_gather}"
+                               + (f", {len(buckets)} length buckets (max_cv={args.max_cv}), "
+                                  "one call pair per bucket" if buckets else ""),
                    "t": w.t, "b": w.b, "s": w.s, "h": w.h, "norm": w.norm, "p": w.p,
                    "n_gather": args.n_gather, "pipeline": args.pipeline,
                    "backward_mask": args.mask, "backward_entry": args.bwd_entry,
@@ -658,10 +745,13 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "timing": "wall clock; copy-in, compute, copy-out pipelined across steps"},
         "gpu_launches": ((3 if fused else 4 + (1 if args.n_gather else 0))
-                         + (1 if (args.bwd_entry == "g" and not fused) else 0)) * args.steps,
+                         + (1 if (args.bwd_entry == "g" and not fused) else 0))
+                        * (len(buckets) if buckets else 1) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if bucketing is not None:
+        line["bucketing"] = bucketing
     if rejected:
         line["clocks_remeasured"] = True
     print(json.dumps(line), flush=True)
@@ -698,6 +788,7 @@ def run_reference(args):
                                f"s={w.s}, h={w.h}, p={w.p}, n_gather=1 (sampled: {procs} x "
                                f"{n_tok} tokens per step)", "t": w.t, "s": w.s, "h": w.h},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": procs, "kind": "oracle",
+                         "nproc": os.cpu_count(),
                          "sample": f"{procs} oracle processes (one per host core) x {n_tok} "
                                    f"tokens per step of the {w.name} shape"},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -730,6 +821,12 @@ def parse_args(argv=None):
                     help="regen: the backward draws the dropout mask again (mask-free)")
     ap.add_argument("--pipeline", choices=["fused", "unfused"], default="fused",
                     help="unfused: reduce-scatter, shard norm and all-gather as three calls")
+    ap.add_argument("--bucket", action="store_true",
+                    help="packed workload: bucket its sequences by length (bucket_by_tokens) "
+                         "and run the boundary once per bucket; the unbucketed batch is timed "
+                         "beside it")
+    ap.add_argument("--max-cv", type=float, default=0.15,
+                    help="length-CV bound of a bucket (with --bucket)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

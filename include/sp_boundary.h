@@ -241,9 +241,13 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z,
  *    SP_NOALLOC_WORKSPACE_BYTES are rejected with SP_ERR_UNSUPPORTED before
  *    anything is enqueued.  h = 8192 (152 blocks on a 152-SM GPU) fits;
  *    h = 5120 (304 blocks) and h = 16384 do not.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress); make that first call before any stream capture
- *    on that device.
+ *  - Outside stream capture every call looks up the array's device address
+ *    on the current device (cudaGetSymbolAddress, a host-side query), so an
+ *    address that changed after cudaDeviceReset is picked up; a call made
+ *    while `stream` is being captured reuses the address of the device's
+ *    last uncaptured call instead.  Make the first call on each device (and
+ *    the first after a cudaDeviceReset) before any stream capture on it; a
+ *    captured first call returns SP_ERR_INVALID_ARG.
  *  - All calls on a device share the one array: calls that may overlap on the
  *    GPU (different streams, no ordering between them) race on it.  Serialise
  *    them (one stream, or events).  Every call overwrites the partials it

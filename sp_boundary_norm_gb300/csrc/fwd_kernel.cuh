@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
   __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
   __shared__ __align__(8) uint64_t xbar[2];   // CL > 1: the partner's row sums arrived
   __shared__ __align__(8) float2 xpub[2];     // CL > 1: this CTA's row sums, published
+  __shared__ int abort_flag;   // nonzero once any thread of the block gave up a wait
   constexpr int kWarps = NTHR / 32;   // compute warps; warp kWarps issues the copies
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       mbar_init(&xbar[0], 1);
       mbar_init(&xbar[1], 1);
     }
+    abort_flag = 0;
     mbar_fence_init();
   }
   if (CL > 1)
@@ -79,30 +81,44 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
   const int64_t c0 = tid * 8;   // this thread's first channel in every chunk
 
   // ---- producer warp: stage every (row, chunk) item in order ------------
-  // Item j goes to stage j % STAGES as soon as the compute warps have
-  // released the stage's previous item (they do so right after reading it,
-  // so a stage refills while the previous chunk is still being computed);
-  // lane 0 arms the stage's full barrier with the item's byte count and
-  // issues one bulk copy per stream.  After a wait times out a thread stops
-  // waiting (its later data may be wrong; the call reports SP_ERR_TIMEOUT),
-  // so a broken pipeline costs about one wait limit, not one per item.
-  bool timed_out = false;
+  // Lane 0 of the producer warp stages item j into stage j % STAGES as soon as
+  // the compute warps have released the stage's previous item (they do so
+  // right after reading it, so a stage refills while the previous chunk is
+  // still being computed): it arms the stage's full barrier with the item's
+  // byte count and issues one bulk copy per stream.
+  // Giving up is well defined: a thread whose wait runs out raises the
+  // block's abort flag; from then on no thread waits on, reads or releases a
+  // stage, the producer issues nothing more, and before the block ends it
+  // waits (bounded) for exactly the copies it did issue, so no copy lands in
+  // shared memory after the block has gone.  The call then reports
+  // SP_ERR_TIMEOUT and its outputs are undefined.
+  volatile int* const abort_v = &abort_flag;
+  bool timed_out = false;   // this thread's own wait ran out
   if (tid >= NTHR) {
-    RowWalk pf;
-    pf.init(P.map, r0);
-    int64_t item = 0;
-    for (int64_t ri = 0; ri < nrows; ++ri) {
-      if (ri > 0) pf.next(P.map, step);
-      const int64_t goff = pf.row * h + coff, roff = pf.local * h + coff;
-      const int kk = pf.k;
-      for (int ch = 0; ch < nchunk; ++ch, ++item) {
-        const int s = static_cast<int>(item % STAGES);
-        const int64_t use = item / STAGES;
-        if (use > 0 && !timed_out &&
-            !mbar_wait(&bar_empty[s], static_cast<uint32_t>((use - 1) & 1)))
-          timed_out = true;
-        const bool withheld = P.withhold != 0 && blockIdx.x == 0 && item == 0;   // test hook
-        if (lane == 0 && !withheld) {
+    if (lane == 0) {
+      RowWalk pf;
+      pf.init(P.map, r0);
+      int64_t item = 0;   // items attempted so far, in order; all but a withheld one issued
+      for (int64_t ri = 0; ri < nrows && *abort_v == 0; ++ri) {
+        if (ri > 0) pf.next(P.map, step);
+        const int64_t goff = pf.row * h + coff, roff = pf.local * h + coff;
+        const int kk = pf.k;
+        int ch = 0;
+        for (; ch < nchunk; ++ch, ++item) {
+          const int s = static_cast<int>(item % STAGES);
+          const int64_t use = item / STAGES;
+          if (use > 0) {
+            const int r = mbar_wait_or_abort(&bar_empty[s], static_cast<uint32_t>((use - 1) & 1),
+                                             abort_v);
+            if (r != kWaitDone) {
+              if (r == kWaitTimedOut) {
+                timed_out = true;
+                *abort_v = 1;
+              }
+              break;
+            }
+          }
+          if (P.withhold != 0 && blockIdx.x == 0 && item == 0) continue;   // test hook
           const int cc = ch * kChunk;
           const int n = (hl - cc < kChunk) ? static_cast<int>(hl - cc) : kChunk;
           const uint32_t bytes = static_cast<uint32_t>(n) * 2u;
@@ -118,21 +134,27 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
           }
           bulk_g2s(dst + t * kStream, P.residual[kk] + roff + cc, bytes, &bar_full[s]);
         }
-        __syncwarp();
+        if (ch < nchunk) break;   // gave up
       }
+      // Drain: the copies of the last STAGES items issued must land before the
+      // block may end.  Item j was issued only after the stage's previous
+      // item had completed its phase, so its copies complete phase
+      // (j / STAGES) & 1 of its stage; a withheld item issued nothing.
+      for (int64_t j = (item > STAGES ? item - STAGES : 0); j < item; ++j) {
+        if (P.withhold != 0 && blockIdx.x == 0 && j == 0) continue;
+        if (!mbar_wait(&bar_full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1)))
+          timed_out = true;
+      }
+      if (timed_out && P.status != nullptr) *P.status = SP_ERR_TIMEOUT;
     }
-    // the last copies must land before the block may end (bounded even
-    // after a timeout)
-    for (int64_t j = (item > STAGES ? item - STAGES : 0); j < item; ++j)
-      if (!mbar_wait(&bar_full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1)))
-        timed_out = true;
-    if (timed_out && P.status != nullptr) *P.status = SP_ERR_TIMEOUT;
+    __syncwarp();
     if (CL > 1) cluster_sync_all();
     return;
   }
 
   RowWalk cur;
   cur.init(P.map, r0);
+  bool gave_up = false;   // this thread stopped waiting (its wait ran out, or the block aborted)
   int slot_sel = 0;
   const float inv_h = 1.f / static_cast<float>(h);
 
@@ -155,9 +177,17 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
         mbar_arrive_remote(cluster_map(&xbar[slot], peer));
       }
       float2 other = make_float2(0.f, 0.f);
-      if (lane == 0) {
-        if (!timed_out && !mbar_wait_cluster(&xbar[slot], par)) timed_out = true;
-        if (!timed_out) other = ld_cluster_f2(cluster_map(&xpub[slot], peer));
+      if (lane == 0 && !gave_up) {
+        const int r = mbar_wait_cluster_or_abort(&xbar[slot], par, abort_v);
+        if (r == kWaitDone) {
+          other = ld_cluster_f2(cluster_map(&xpub[slot], peer));
+        } else {
+          gave_up = true;
+          if (r == kWaitTimedOut) {
+            timed_out = true;
+            *abort_v = 1;
+          }
+        }
       }
       other.x = __shfl_sync(0xFFFFFFFFu, other.x, 0);
       other.y = __shfl_sync(0xFFFFFFFFu, other.y, 0);
@@ -180,14 +210,25 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     for (int ch = 0; ch < nchunk; ++ch) {
       const int64_t item = ri * nchunk + ch;
       const int stage = static_cast<int>(item % STAGES);
-      if (!timed_out && !mbar_wait(&bar_full[stage], static_cast<uint32_t>((item / STAGES) & 1)))
-        timed_out = true;
+      bool have = false;   // the item has landed and this thread may read it
+      if (!gave_up) {
+        const int r = mbar_wait_or_abort(&bar_full[stage],
+                                         static_cast<uint32_t>((item / STAGES) & 1), abort_v);
+        have = r == kWaitDone;
+        if (!have) {
+          gave_up = true;
+          if (r == kWaitTimedOut) {
+            timed_out = true;
+            *abort_v = 1;
+          }
+        }
+      }
       const int cc = ch * kChunk;
       // g*: float32 sum of the t partials, ranks in ascending order
       // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
-      float y[8];
+      float y[8] = {};
       uint4 rv = make_uint4(0, 0, 0, 0);
-      if (cc + c0 < hl) {
+      if (have && cc + c0 < hl) {
         const uint8_t* slot = smem + stage * stage_bytes + tid * 16;
         unpack8(lds16(slot), y);
         if (!SHARD) {
@@ -198,7 +239,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
         rv = lds16(slot + t * kStream);   // the residual, used after the dropout
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[stage]);   // the stage is free again
+      if (lane == 0 && have) mbar_arrive(&bar_empty[stage]);   // the stage is free again
       if (cc + c0 < hl) {
         const uint4 bv = ldg16(P.bias + coff + cc + c0);
         add8_bf16(bv, y);   // + bias

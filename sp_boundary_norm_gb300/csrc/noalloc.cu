@@ -16,25 +16,35 @@
 namespace {
 
 // Scratch of the allocate-nothing backward, one per GPU that loads the
-// library.  Only its host-side address (looked up per device) is handed to
-// the kernels; the host symbol itself is not a device address.
+// library.  Only its device address, looked up with cudaGetSymbolAddress on
+// the device in question, is handed to the kernels; the host-side symbol
+// itself is not a device address.
 static __device__ __align__(256) float g_noalloc_ws[SP_NOALLOC_WORKSPACE_BYTES / sizeof(float)];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_ws_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_ws on the current device, looked up the first
-// time this device is seen.
-sp_status_t scratch_address(void** out) {
+// Device address of g_noalloc_ws on the current device.  Outside stream
+// capture it is looked up on every call (a host-side query, no device work),
+// so a module reloaded at another address after cudaDeviceReset is seen; the
+// address is remembered per device for calls made while `stream` is being
+// captured, where the lookup is not made.  A device's first call must
+// therefore come before any capture on it.
+sp_status_t scratch_address(cudaStream_t stream, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return spb::record_error(SP_ERR_CUDA, "sp_norm_bwd_noalloc: no usable current device");
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;   // e.g. the legacy stream during a global capture
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ws_addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_ws);
     if (e != cudaSuccess || p == nullptr) {
@@ -43,6 +53,10 @@ sp_status_t scratch_address(void** out) {
                                "sp_norm_bwd_noalloc: cudaGetSymbolAddress of the scratch failed");
     }
     g_ws_addr[dev] = p;
+  } else if (g_ws_addr[dev] == nullptr) {
+    return spb::record_error(SP_ERR_INVALID_ARG,
+                             "sp_norm_bwd_noalloc: the first call on a device must come before "
+                             "any stream capture on it");
   }
   *out = g_ws_addr[dev];
   return SP_OK;
@@ -67,7 +81,7 @@ extern "C" sp_status_t sp_norm_bwd_noalloc(
         "library's fixed SP_NOALLOC_WORKSPACE_BYTES; use sp_norm_bwd with a workspace");
   }
   void* ws = nullptr;
-  const sp_status_t st = scratch_address(&ws);
+  const sp_status_t st = scratch_address(static_cast<cudaStream_t>(stream), &ws);
   if (st != SP_OK) return st;
   // The partials are overwritten in full by every call (nothing is
   // accumulated into the scratch), so it needs no clearing between calls.

@@ -313,6 +313,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
   return true;
 }
 
+// Outcome of a wait that can also be called off by another thread of the
+// block: the phase completed, this thread's own wait ran out (kWaitLimitNs),
+// or another thread had given up first and raised the block's abort flag.
+enum WaitResult { kWaitDone = 0, kWaitTimedOut = 1, kWaitAborted = 2 };
+
+// mbar_wait that also returns as soon as *abort_flag is nonzero.  The flag is
+// read only while the phase is still pending, so a wait that succeeds at once
+// costs the same as mbar_wait.
+__device__ __forceinline__ int mbar_wait_or_abort(uint64_t* b, uint32_t parity,
+                                                  const volatile int* abort_flag) {
+  if (mbar_try_wait(b, parity)) return kWaitDone;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(b, parity)) {
+    if (*abort_flag != 0) return kWaitAborted;
+    if (global_ns() - t0 > kWaitLimitNs) return kWaitTimedOut;
+  }
+  return kWaitDone;
+}
+
 // One contiguous global -> shared copy (16-byte aligned ends, a multiple of
 // 16 bytes), completing on the mbarrier's transaction count.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
@@ -365,13 +384,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* b, uint32_t pari
   return ok != 0;
 }
 
-// Bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity) {
-  if (mbar_try_wait_cluster(b, parity)) return true;
+// Bounded and abortable like mbar_wait_or_abort.
+__device__ __forceinline__ int mbar_wait_cluster_or_abort(uint64_t* b, uint32_t parity,
+                                                          const volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(b, parity)) return kWaitDone;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait_cluster(b, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  return true;
+  while (!mbar_try_wait_cluster(b, parity)) {
+    if (*abort_flag != 0) return kWaitAborted;
+    if (global_ns() - t0 > kWaitLimitNs) return kWaitTimedOut;
+  }
+  return kWaitDone;
 }
 
 __device__ __forceinline__ float2 ld_cluster_f2(uint32_t cluster_addr) {

@@ -116,3 +116,36 @@ def backward_inputs(w, device="cpu", seed=None, with_skip=False):
     skip = ([_normal((w.b, sk, w.h), 1.0, gen, device) for sk in w.shard_sizes()]
             if with_skip else None)
     return {"dy": dy, "dz_skip": skip}
+
+
+def regroup_packed(w, order, lengths, partials, shards):
+    """The sequences ``order`` of a packed workload (b = 1), laid out as a
+    packed batch of their own: what a data loader hands the boundary after
+    it has bucketed the batch by length.
+
+    ``partials`` are the t full (1, T, h) partials; ``shards`` any number of
+    sharded tensor lists (residual, dY, ...) of the original workload.
+    Returns the regrouped workload (its s = the bucket's tokens, its
+    ``seqlens`` = the sequences' lengths in bucket order), its t partials and
+    each shard list re-cut at the new workload's shard offsets.  Values are
+    moved, never computed."""
+    if w.b != 1 or not w.ragged:
+        raise ValueError("regrouping needs a packed workload (b == 1, seqlens)")
+    cu = [0]
+    for n in w.seqlens:
+        cu.append(cu[-1] + int(n))
+    for i, n in zip(order, lengths):
+        if cu[i + 1] - cu[i] != int(n):
+            raise ValueError(f"sequence {i} has {cu[i + 1] - cu[i]} tokens, not {n}")
+
+    def pick(full):
+        return torch.cat([full[:, cu[i]:cu[i + 1]] for i in order], dim=1).contiguous()
+
+    wb = w.with_(s=int(sum(int(n) for n in lengths)), seqlens=tuple(int(n) for n in lengths))
+    parts = [pick(P) for P in partials]
+    out = []
+    for lst in shards:
+        full = pick(torch.cat(list(lst), dim=1))
+        o = [(k * wb.s) // wb.t for k in range(wb.t + 1)]
+        out.append([full[:, o[k]:o[k + 1]].contiguous() for k in range(wb.t)])
+    return wb, parts, out

@@ -67,3 +67,41 @@ def test_invalid_arguments():
         bk.bucket_by_tokens([1, -2])
     with pytest.raises(ValueError):
         bk.bucket_by_tokens([1, 2], max_tokens=0)
+
+
+def test_regroup_packed_moves_whole_sequences_and_reshards():
+    import torch
+    lens = (5, 17, 3, 40, 1, 9)
+    w = wl.Workload("rg", t=4, b=1, s=sum(lens), h=8, seqlens=lens, draw_seed=3)
+    inp = wl.forward_inputs(w, "cpu")
+    dy = wl.backward_inputs(w, "cpu")["dy"]
+    cu = wl.cu_seqlens(lens)
+    order, blens = (3, 0, 5), (40, 5, 9)
+    wb, parts, (res, dyb) = wl.regroup_packed(w, order, blens, inp["partials"],
+                                              [inp["residual"], dy])
+    assert wb.s == 54 and wb.seqlens == blens and wb.t == w.t
+    assert [x.shape[1] for x in res] == wb.shard_sizes() == [x.shape[1] for x in dyb]
+    full_res = torch.cat(inp["residual"], dim=1)
+    got_res = torch.cat(res, dim=1)
+    pos = 0
+    for i, n in zip(order, blens):
+        assert torch.equal(got_res[:, pos:pos + n], full_res[:, cu[i]:cu[i + 1]])
+        for P, Pb in zip(inp["partials"], parts):
+            assert torch.equal(Pb[:, pos:pos + n], P[:, cu[i]:cu[i + 1]])
+        pos += n
+    with pytest.raises(ValueError):
+        wl.regroup_packed(w, (3,), (41,), inp["partials"], [])
+    with pytest.raises(ValueError):
+        wl.regroup_packed(w.with_(seqlens=()), (0,), (5,), inp["partials"], [])
+
+
+def test_regroup_packed_of_the_buckets_covers_every_token_once():
+    import torch
+    w = wl.WORKLOADS["ragged"].with_(h=8)
+    inp = wl.forward_inputs(w, "cpu")
+    tok = torch.arange(w.s, dtype=torch.float32).reshape(1, -1, 1).expand(1, w.s, 8)
+    seen = []
+    for b in bk.bucket_by_tokens(w.seqlens, max_cv=0.15):
+        _, parts, _ = wl.regroup_packed(w, b.indices, b.lengths, [tok], [])
+        seen.append(parts[0][0, :, 0])
+    assert torch.equal(torch.sort(torch.cat(seen)).values, torch.arange(w.s, dtype=torch.float32))

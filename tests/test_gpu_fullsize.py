@@ -1,0 +1,130 @@
+"""Full-size parity: every element of the full-size workloads against the oracle.
+
+The 70B-shape forward (LayerNorm, and the RMSNorm workload of the backward
+configuration) and the packed workload (42,823 tokens, h = 5120) run in the
+launch configuration the benchmark times (one gathered copy); Z and the
+dropout mask are compared bit for bit on every element, mean / rstd on every
+token, and the gathered O on every element at the bf16 bar.  The backward of
+the same workloads is compared on every dResidual and dYpre element, and its
+parameter gradients summed over every token.  "第 7 课：序列并行 SP" §3: the
+token-wise operators give the same result whichever rank holds a token, so
+the sharded outputs must equal the oracle's per-token results everywhere;
+answer to Q1: the masks agree element for element.
+
+The oracle runs over chunks of tokens in a thread pool on the host cores
+(see ``_cases.full_fwd_check``); each test prints its counts, including how
+many elements passed through the magnitude floor alone.
+"""
+import time
+
+import pytest
+import torch
+
+from sp_boundary_norm_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("_cases")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+
+
+@pytest.mark.parametrize("name", ["70b", "bwd70b_rms", "ragged"])
+def test_forward_full_size_every_element(name):
+    w = wl.WORKLOADS[name]
+    inp = wl.forward_inputs(w, C.DEV)
+    out = C.run_fwd(w, inp, n_gather=1)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    t0 = time.perf_counter()
+    tot = C.full_fwd_check(w, inp, out)
+    print(f"\nfull-size forward {name}: {tot} ({time.perf_counter() - t0:.1f} s, "
+          f"{C.host_threads()} threads)")
+
+
+@pytest.mark.parametrize("name", ["bwd70b", "bwd70b_rms", "ragged"])
+def test_backward_full_size_every_element(name):
+    w = wl.WORKLOADS[name]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    out = C.run_bwd(w, fwd, inp["gamma"], dy, None, n_gather=1)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    t0 = time.perf_counter()
+    tot = C.full_bwd_check(w, fwd, inp["gamma"], dy, None, out)
+    print(f"\nfull-size backward {name}: {tot} ({time.perf_counter() - t0:.1f} s, "
+          f"{C.host_threads()} threads)")
+
+
+@pytest.mark.parametrize("name", ["bwd70b", "ragged"])
+def test_mask_free_backward_full_size_every_element(name):
+    """The mask-free backward at full size, every element against the oracle
+    run with the forward's stored mask: the keep decisions it draws again
+    must be the forward's (answer to Q1: one seed, the same mask everywhere).
+    At h = 8192 it runs its own launch shape (256 threads x 4 chunks, terms in
+    tensor memory), so its float32 row sums may round differently from the
+    stored-mask backward's; the bar is the oracle's, not bit equality."""
+    w = wl.WORKLOADS[name]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    got = C.alloc_bwd(w, 1)
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+    C.sp.sp_norm_bwd_philox(dy, fwd["z"], fwd["mean"], fwd["rstd"], inp["gamma"], None, s=w.s,
+                            p=w.p, seed=w.seed, offset=w.offset, norm=w.norm, cu_seqlens=cu,
+                            dresidual=got["dres"], dgathered=got["dgat"], dgamma=got["dgamma"],
+                            dbeta=got["dbeta"], dbias=got["dbias"], workspace=got["ws"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    t0 = time.perf_counter()
+    tot = C.full_bwd_check(w, fwd, inp["gamma"], dy, None, got)
+    print(f"\nfull-size mask-free backward {name}: {tot} ({time.perf_counter() - t0:.1f} s)")
+
+
+def test_rs_norm_bwd_full_size_every_element():
+    """The backward entered through g at the 70B shape: dY is the float32
+    rank-ascending sum of the t ranks' partial gradients of the gathered
+    input (the reduce-scatter that is the gradient of g, "第 7 课" §3.B),
+    fused into the norm backward; every element against the oracle."""
+    w = wl.WORKLOADS["bwd70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(97, C.DEV)
+    parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=C.DEV) * 0.35).to(torch.bfloat16)
+             for _ in range(w.t)]
+    out = C.alloc_bwd(w, 1)
+    C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                        None, p=w.p, norm=w.norm, dresidual=out["dres"], dgathered=out["dgat"],
+                        dgamma=out["dgamma"], dbeta=out["dbeta"], dbias=out["dbias"],
+                        workspace=out["ws"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    t0 = time.perf_counter()
+    tot = C.full_bwd_check(w, fwd, inp["gamma"], None, None, out, dy_partials=parts)
+    print(f"\nfull-size backward through g: {tot} ({time.perf_counter() - t0:.1f} s)")
+
+
+def test_70b_one_gathered_copy_per_rank_every_element():
+    """n_gather = t at the 70B shape (the --n-gather 8 bench line): every
+    element of every rank's gathered O and gathered dYpre against the oracle."""
+    w = wl.WORKLOADS["70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=w.t)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    t0 = time.perf_counter()
+    f = C.full_fwd_check(w, inp, fwd)
+    del fwd["gathered"]
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    out = C.run_bwd(w, fwd, inp["gamma"], dy, None, n_gather=w.t)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    g = C.full_bwd_check(w, fwd, inp["gamma"], dy, None, out)
+    print(f"\nfull-size n_gather={w.t}: forward {f}, backward {g} "
+          f"({time.perf_counter() - t0:.1f} s)")

@@ -41,8 +41,7 @@ def _full_fwd_compare(w, inp, out):
                                         C.f32(inp["beta"]), w.eps, w.norm)[3].reshape(z.shape)
                           for z in ref["z"]], axis=1)
     for j, g in enumerate(out["gathered"]):
-        bad = compare.bf16_mismatch(compare.bf16_bits(g), out_exact, mag)
-        assert not bad.any(), f"gathered[{j}]: {bad.sum()} off"
+        C.assert_bf16(compare.bf16_bits(g), out_exact, mag, f"gathered[{j}]")
     return ref
 
 
@@ -80,9 +79,8 @@ def test_forward_equals_unsharded_path_sliced_by_token(variant):
         if w.norm == "layernorm":
             assert not compare.f32_rel_mismatch(out["mean"][k].cpu().numpy(),
                                                 ref["mean"][:, sl]).any()
-    bad = compare.bf16_mismatch(compare.bf16_bits(out["gathered"][0]), ref["out_exact"],
-                                ref["out_magnitude"])
-    assert not bad.any(), f"{bad.sum()} elements off"
+    C.assert_bf16(compare.bf16_bits(out["gathered"][0]), ref["out_exact"], ref["out_magnitude"],
+                  "gathered[0]")
 
 
 @pytest.fixture
@@ -603,7 +601,7 @@ def test_unfused_pipeline_matches_oracle(variant):
         assert not compare.f32_rel_mismatch(out["rstd"][k].cpu().numpy(), ref["rstd"][k]).any()
         mag = ob._norm_rows(ref["z"][k].reshape(-1, w.h).astype(np.float64), C.f32(inp["gamma"]),
                             C.f32(inp["beta"]), w.eps, w.norm)[3].reshape(ref["z"][k].shape)
-        assert not compare.bf16_mismatch(compare.bf16_bits(o[k]), ref["out_exact"][k], mag).any()
+        C.assert_bf16(compare.bf16_bits(o[k]), ref["out_exact"][k], mag, f"o[{k}]")
     full = np.concatenate(ref["out"], axis=1)
     got = compare.bf16_bits(out["gathered"][0])
     # the gathered copy is the shards' O laid out along s (bit-exact copy of o)
@@ -645,7 +643,7 @@ def test_unfused_pipeline_70b_sampled():
     mu = np.array([float(out["mean"][k].reshape(-1)[l]) for k, l in locs])
     assert not compare.f32_rel_mismatch(mu, ref["mean"]).any(), "mean"
     got_o = np.stack([compare.bf16_bits(row(o, k, l)) for k, l in locs])
-    assert not compare.bf16_mismatch(got_o, ref["out_exact"], ref["out_magnitude"]).any(), "O"
+    C.assert_bf16(got_o, ref["out_exact"], ref["out_magnitude"], "O")
     g = compare.bf16_bits(out["gathered"][0].reshape(-1, w.h).index_select(0, toks))
     assert np.array_equal(g, got_o), "gathered rows are the shards' O"
 
@@ -828,13 +826,11 @@ def _rs_bwd_check(w, fwd, inp, parts, skip, out, tokens=None):
                                None if skip is None else C.f32(rows(skip)), p=w.p, norm=w.norm)
         sel = np.arange(n) if tokens is None else tokens[(tokens >= 0) & (tokens < n)]
         dres = compare.bf16_bits(out["dres"][k].reshape(-1, h))
-        bad = compare.bf16_mismatch(dres[sel], one["dz"][sel], one["dz_magnitude"][sel])
-        assert not bad.any(), f"dresidual[{k}]: {bad.sum()} off"
+        C.assert_bf16(dres[sel], one["dz"][sel], one["dz_magnitude"][sel], f"dresidual[{k}]")
         for j, dg in enumerate(out["dgat"]):
             blk = compare.bf16_bits(dg[:, offs[k]:offs[k + 1], :].reshape(-1, h))
-            bad = compare.bf16_mismatch(blk[sel], one["dypre_exact"][sel],
-                                        one["dz_magnitude"][sel] * scale)
-            assert not bad.any(), f"dgathered[{j}] shard {k}: {bad.sum()} off"
+            C.assert_bf16(blk[sel], one["dypre_exact"][sel], one["dz_magnitude"][sel] * scale,
+                          f"dgathered[{j}] shard {k}")
         for name in acc:
             terms = one[name + "_terms"]
             if terms is not None:
