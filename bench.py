@@ -77,6 +77,17 @@ def bwd_bytes_per_token(h, n_gather, norm="layernorm", skip=False):
     return 2 * h + 2 * h + h + stats + (2 * h if skip else 0) + 2 * h + 2 * h * n_gather
 
 
+def launches_per_step(fused, n_gather, bwd_entry):
+    """Kernels of this library one step launches.  Forward: the fused kernel,
+    or reduce-scatter + shard norm (+ all-gather).  Backward: the norm
+    backward (fused with the reduce-scatter when entered through g) and the
+    parameter-gradient reduce; entered through g unfused, a separate
+    reduce-scatter first."""
+    fwd = 1 if fused else 2 + (1 if n_gather else 0)
+    bwd = 2 + (1 if (bwd_entry == "g" and not fused) else 0)
+    return fwd + bwd
+
+
 # ---------------------------------------------------------- distributed --
 
 def dist_env():
@@ -744,8 +755,7 @@ def run_ours(args):
         "e2e": {"value": round(w.tokens * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "timing": "wall clock; copy-in, compute, copy-out pipelined across steps"},
-        "gpu_launches": ((3 if fused else 4 + (1 if args.n_gather else 0))
-                         + (1 if (args.bwd_entry == "g" and not fused) else 0))
+        "gpu_launches": launches_per_step(fused, args.n_gather, args.bwd_entry)
                         * (len(buckets) if buckets else 1) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -973,3 +973,5 @@ def test_default_launch_shapes(h, fwd_threads, bwd_shape):
     assert f["threads"] == fwd_threads and f["cluster"] == 1, f
     b = C.sp.sp_debug_last_shape(1)
     assert (b["threads"], b["chunks"]) == bwd_shape, b
+    if h == 8192:
+        assert b["stages"] == 3, b   # one block per SM stages three rows
