@@ -434,20 +434,25 @@ LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip)
                     [&](int st) { return rs_bwd_kernel(threads, maxc, t, st); });
 }
 
-LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool regen) {
+// bulk: dYpre sent to the gathered copies by bulk copies from two shared
+// copies of the row (stored mask only), for calls with several copies.
+LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool regen, bool bulk) {
   int threads, maxc;
   bwd_threads(h, regen, &threads, &maxc);
   const size_t item =
       static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
   const size_t ring_row = item * maxc;
+  const size_t stage_row = static_cast<size_t>((h * 2 + 15) / 16) * 16;
+  const size_t fixed = 2 * 32 * sizeof(float2) + (bulk ? 2 * stage_row : 0);
   const bool tacc = bwd_tmem_shape(threads, maxc);
   const int cap = tacc ? 512 / bwd_tmem_cols(threads, maxc) : (threads <= 256 ? 512 / threads : 1);
   // rows staged: three when one block holds the SM (measured on GB300, h = 8192:
   // 0.191 against 0.194 ms), else two
-  LaunchShape ls = pick_shape(1, threads, maxc, rows, ring_row, 2 * 32 * sizeof(float2), kBwdRing,
+  LaunchShape ls = pick_shape(1, threads, maxc, rows, ring_row, fixed, kBwdRing,
                               3, /*ring=*/cap == 1 ? 3 : 2, /*blocks per SM=*/cap, [&](int st) {
                                 return regen ? bwd_regen_kernel(threads, maxc, st)
-                                             : bwd_kernel(threads, maxc, st);
+                                             : bulk ? bwd_bulk_kernel(threads, maxc, st)
+                                                    : bwd_kernel(threads, maxc, st);
                               });
   if (tacc && ls.fits) {
     // The blocks of an SM share its 512 tensor-memory columns: pad the shared
@@ -475,9 +480,10 @@ LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
                       [&] { return rs_bwd_shape_uncached(rows, h, t, has_skip); });
 }
 
-LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false) {
-  return cached_shape(3, rows, h, 0, (has_skip ? 1 : 0) | (regen ? 2 : 0),
-                      [&] { return bwd_shape_uncached(rows, h, has_skip, regen); });
+LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false,
+                      bool bulk = false) {
+  return cached_shape(3, rows, h, 0, (has_skip ? 1 : 0) | (regen ? 2 : 0) | (bulk ? 4 : 0),
+                      [&] { return bwd_shape_uncached(rows, h, has_skip, regen, bulk); });
 }
 
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
@@ -790,8 +796,8 @@ size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, s
   // the largest grid over the variants (skip gradient or not, stored or
   // regenerated mask): one workspace size serves every backward entry point
   int grid = 0;
-  for (int v = 0; v < 4; ++v) {
-    const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v & 2) != 0);
+  for (int v = 0; v < 6; ++v) {   // skip gradient or not; stored, regenerated or bulk
+    const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v >> 1) == 1, (v >> 1) == 2);
     if (ls.grid > grid) grid = ls.grid;
   }
   if (h <= 8192) {
@@ -848,7 +854,13 @@ static sp_status_t norm_bwd_common(
     return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
 
   const bool has_skip = dz_skip != nullptr;
-  const LaunchShape ls = bwd_shape(rows, h, has_skip, regen);
+  // several gathered copies: the bulk-copy variant, if its shape fits
+  bool bulk = !regen && n_gather > 1;
+  LaunchShape ls = bwd_shape(rows, h, has_skip, regen, bulk);
+  if (bulk && !ls.fits) {
+    bulk = false;
+    ls = bwd_shape(rows, h, has_skip, regen, false);
+  }
   g_last_shape[1] = ls;
   const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need)
@@ -906,7 +918,8 @@ static sp_status_t norm_bwd_common(
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const void* fn = regen ? bwd_regen_kernel(ls.threads, ls.maxc, ls.stages)
-                         : bwd_kernel(ls.threads, ls.maxc, ls.stages);
+                   : bulk  ? bwd_bulk_kernel(ls.threads, ls.maxc, ls.stages)
+                           : bwd_kernel(ls.threads, ls.maxc, ls.stages);
   cudaError_t e = launch(fn, ls, &P, cs);
   if (e != cudaSuccess) return fail_cuda(e, "sp_norm_bwd launch");
   if (dgamma || (dbeta && ln) || dbias) {

@@ -13,7 +13,15 @@ namespace spb {
 // dbias terms in tensor memory (its lane, 24 columns per chunk), which frees
 // the registers for wider rows per thread at 16 warps per SM; the others keep
 // them in registers.
-template <int NTHR, int MAXC, int RING, bool REGEN>
+// BULK = true (used when dYpre goes to several gathered copies): each thread
+// writes its dYpre values once, into a shared-memory copy of the row (two
+// such rows, alternating), and thread 0 sends the whole row to every
+// gathered copy with bulk copies (one per copy, h * 2 bytes each) right
+// after the next row's block barrier, so the threads issue one shared store
+// instead of n_gather global stores per 8 elements and no barrier is added.
+// A row buffer is rewritten two rows later, after thread 0 has seen its
+// copies finish reading it (before that row's barrier).
+template <int NTHR, int MAXC, int RING, bool REGEN, bool BULK = false>
 __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
                                             ? 512 / bwd_tmem_cols(NTHR, MAXC)
                                             : (NTHR <= 256 ? 512 / NTHR : 1))
@@ -51,6 +59,9 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
   const int item_bytes = off_skip + (has_skip ? v16 : 0);
   const int row_bytes = MAXC * item_bytes;
   float2* red = reinterpret_cast<float2*>(smem + RING * row_bytes);   // [2][32]
+  // BULK: two shared copies of a row's dYpre, h bf16 each (16-byte aligned)
+  uint8_t* const stage0 = smem + RING * row_bytes + 2 * 32 * sizeof(float2);
+  const int stage_bytes = ((h * 2 + 15) / 16) * 16;
   const int c0 = tid * 8;
   uint32_t valid = 0;   // bit ch: this thread has channels in chunk ch
 #pragma unroll
@@ -123,6 +134,7 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
 
   int slot_sel = 0;
   int slot = 0;   // ring slot of the current row
+  int64_t prev_grow = 0;   // BULK: first element of the previous row in the gathered buffers
   const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
     // row ri + RING - 1 refills the slot row ri - 1 used
@@ -183,8 +195,18 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
       }
     }
 
+    // BULK: the copies of row ri - 2 must have read their row buffer before
+    // this barrier (row ri writes it again after it); row ri - 1, complete
+    // in its buffer once every thread has passed the barrier, is sent after it
+    if (BULK && tid == 0) bulk_wait_read_all();
     const float2 s = block_sum2(s1a + s1b, s2a + s2b, red + 32 * slot_sel);
     slot_sel ^= 1;
+    if (BULK && tid == 0 && ri > 0) {
+      const uint8_t* src = stage0 + ((ri - 1) & 1) * stage_bytes;
+      for (int j = 0; j < P.n_gather; ++j)
+        bulk_s2g(P.dgathered[j] + prev_grow, src, static_cast<uint32_t>(h) * 2u);
+      bulk_commit();
+    }
     const float nm1 = is_ln ? -(s.x * inv_h) : 0.f;
     const float nm2r = -(s.y * inv_h) * rstd;
 
@@ -193,6 +215,7 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
     uint16_t* dres_row = P.dresidual[k] + local * h + c0;
     const int64_t grow = row * h + c0;
     uint16_t* dg0_row = P.n_gather > 0 ? P.dgathered[0] + grow : nullptr;
+    uint8_t* const stage_row = stage0 + (ri & 1) * stage_bytes + tid * 16;
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
       float bt[8];   // this chunk's dbias terms
@@ -206,8 +229,9 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
         const uint8_t* it = it0 + ch * item_bytes;
         const uint4 dyv = lds16(it);
         const uint4 zv = lds16(it + v16);
-        uint2 mk;
+        bool kept[8];   // the forward's keep decisions of these 8 elements
         if (REGEN) {
+          // drawn again: element e is kept iff its Philox word >= thr
           const uint64_t q = static_cast<uint64_t>(grow + ch * kChunk) >> 2;
           const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
                                                    static_cast<uint32_t>(q >> 32), P.off0, P.off1),
@@ -216,9 +240,15 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
                                                    static_cast<uint32_t>((q + 1) >> 32), P.off0,
                                                    P.off1),
                                         P.rk);
-          mk = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
+          const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) kept[e] = u[e] >= P.thr;
         } else {
-          mk = lds8(it + off_mask - tid * 8);
+          // stored mask bytes are 0 or 1: bit 0 of byte e decides
+          const uint2 mk = lds8(it + off_mask - tid * 8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            kept[e] = ((e < 4 ? mk.x : mk.y) & (1u << (8 * (e & 3)))) != 0u;
         }
         float zc[8], dz[8], dp[8];
         add8_bf16_bcast(zv, nmean, zc);           // z - mean
@@ -232,17 +262,18 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
 #pragma unroll
         for (int e = 0; e < 8; e += 2) mul2_to(dz[e], dz[e + 1], P.scale, dp[e], dp[e + 1]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          // mask bytes are 0 or 1: bit 0 of byte e decides
-          const bool kept = ((e < 4 ? mk.x : mk.y) & (1u << (8 * (e & 3)))) != 0u;
-          dp[e] = kept ? dp[e] : 0.f;
-        }
+        for (int e = 0; e < 8; ++e) dp[e] = kept[e] ? dp[e] : 0.f;
 #pragma unroll
         for (int e = 0; e < 8; e += 2) add2(bt[e], bt[e + 1], dp[e], dp[e + 1]);
         st16_stream(dres_row + ch * kChunk, pack8(dz));
         const uint4 pb = pack8(dp);
-        if (dg0_row != nullptr) st16_stream(dg0_row + ch * kChunk, pb);
-        for (int j = 1; j < P.n_gather; ++j) st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
+        if (BULK) {
+          *reinterpret_cast<uint4*>(stage_row + ch * (NTHR * 16)) = pb;
+        } else {
+          if (dg0_row != nullptr) st16_stream(dg0_row + ch * kChunk, pb);
+          for (int j = 1; j < P.n_gather; ++j)
+            st16_stream(P.dgathered[j] + grow + ch * kChunk, pb);
+        }
       }
       if constexpr (TACC) {
         tmem_st8(tacc + 24 * ch + 16, bt);
@@ -250,6 +281,24 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc_bias[ch][e] = bt[e];
       }
+    }
+    if (BULK) {
+      fence_proxy_async_smem();   // this row's shared dYpre, visible to the copy engine
+      prev_grow = row * h;
+    }
+  }
+  if (BULK) {
+    // the last row: every thread has written and fenced its part
+    __syncthreads();
+    if (tid == 0) {
+      if (nrows > 0) {
+        bulk_wait_read_all();
+        const uint8_t* src = stage0 + ((nrows - 1) & 1) * stage_bytes;
+        for (int j = 0; j < P.n_gather; ++j)
+          bulk_s2g(P.dgathered[j] + prev_grow, src, static_cast<uint32_t>(h) * 2u);
+        bulk_commit();
+      }
+      bulk_wait_all();   // no copy may still read this block's shared memory at exit
     }
   }
   cp_async_wait<0>();

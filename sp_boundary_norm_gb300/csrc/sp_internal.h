@@ -152,6 +152,8 @@ const void* fwd_kernel_pair(int threads, int t, int stages);
 const void* fwd_shard_kernel(int threads, int stages);
 const void* bwd_kernel(int threads, int maxc, int ring);
 const void* bwd_regen_kernel(int threads, int maxc, int ring);
+// The stored-mask backward sending dYpre to its gathered copies with bulk copies.
+const void* bwd_bulk_kernel(int threads, int maxc, int ring);
 // Backward entered through g (reduce-scatter of t partial gradients fused):
 // (threads, chunks per row, ranks t, chunk stages).
 const void* rs_bwd_kernel(int threads, int maxc, int t, int stages);

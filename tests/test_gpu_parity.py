@@ -470,6 +470,63 @@ def test_70b_one_gathered_copy_per_rank():
         assert torch.equal(g.view(torch.int16), out["dgat"][0].view(torch.int16))
 
 
+@pytest.mark.parametrize("variant,n_gather", [
+    (dict(), 2),
+    (dict(s=4096), 3),                       # several rows per block: both row buffers reused
+    (dict(t=8, s=64, h=8192), 8),            # the 70B row width, one row per block
+    (dict(t=8, s=4096, h=8192), 8),
+    (dict(t=8, s=512, h=5120), 4),           # the tensor-memory shape
+    (dict(t=8, s=1024, h=4096, norm="rmsnorm", eps=1e-6), 2),
+    (dict(skip=True, s=1000), 5),
+    (dict(seqlens=(300, 17, 683), s=1000, t=3), 3),
+])
+def test_backward_bulk_gathered_copies_equal_per_thread_stores(variant, n_gather):
+    """With several gathered copies the backward writes each row's dYpre once
+    into shared memory and sends it to every copy with bulk copies.  Every
+    copy must equal, bit for bit, the copy the per-thread stores write with a
+    single gathered copy; dResidual and the parameter gradients are
+    unchanged; nothing outside the copies is written."""
+    v = dict(variant)
+    skip = v.pop("skip", False)
+    w = wl.Workload("bk", t=2, b=1, s=256, h=512, draw_seed=37).with_(**v)
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    bi = wl.backward_inputs(w, C.DEV, with_skip=skip)
+    one = C.run_bwd(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], n_gather=1)
+    torch.cuda.synchronize()
+    shape_one = C.sp.sp_debug_last_shape(1)
+    pad = 4096
+    nbytes = w.tokens * w.h * 2
+    raws = [torch.full((nbytes + 2 * pad,), 0x5A, dtype=torch.uint8, device=C.DEV)
+            for _ in range(n_gather)]
+    for raw in raws:
+        raw[pad:pad + nbytes] = 0xFF   # NaN bf16 pattern: every element must be written
+    out = C.alloc_bwd(w, 0)
+    out["dgat"] = [raw[pad:pad + nbytes].view(torch.bfloat16).view(w.b, w.s, w.h) for raw in raws]
+    C.run_bwd(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], out=out)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    shape_many = C.sp.sp_debug_last_shape(1)
+    stage = ((w.h * 2 + 15) // 16) * 16
+    tmem = (shape_many["threads"], shape_many["chunks"]) in ((320, 2), (256, 4), (128, 4))
+    if not tmem:   # (tensor-memory shapes pad their shared memory to a fixed size)
+        assert shape_many["smem"] >= shape_one["smem"] + 2 * stage or shape_many["stages"] != \
+            shape_one["stages"], (shape_one, shape_many)   # the bulk variant ran
+    ref = one["dgat"][0].view(torch.int16)
+    for g in out["dgat"]:
+        assert torch.equal(g.view(torch.int16), ref)
+    for raw in raws:
+        assert bool((raw[:pad] == 0x5A).all()) and bool((raw[-pad:] == 0x5A).all())
+    for a, b in zip(out["dres"], one["dres"]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    names = ["dgamma", "dbias"] + (["dbeta"] if w.norm == "layernorm" else [])
+    for name in names:
+        if shape_many["grid"] == shape_one["grid"]:
+            assert torch.equal(out[name], one[name]), name
+        else:
+            assert torch.allclose(out[name], one[name], rtol=1e-5, atol=1e-4), name
+
+
 def test_backward_ragged_workload_sampled_and_param_grads():
     """The packed workload at full size in the bench's launch configuration
     (h = 5120 runs the tensor-memory shape, 320 threads x 2 chunks):
