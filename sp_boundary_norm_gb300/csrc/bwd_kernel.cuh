@@ -216,8 +216,31 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
     const int64_t grow = row * h + c0;
     uint16_t* dg0_row = P.n_gather > 0 ? P.dgathered[0] + grow : nullptr;
     uint8_t* const stage_row = stage0 + (ri & 1) * stage_bytes + tid * 16;
+    // REGEN: Philox words [chunk of the group][call].  In the shapes whose
+    // parameter-gradient terms live in tensor memory the draws of two chunks
+    // are made together (four independent Philox chains in flight instead of
+    // two); the register shapes have no registers to spare for it, and each
+    // chunk draws its own.
+    constexpr int kDrawGroup = (TACC && MAXC >= 2) ? 2 : 1;
+    uint4 draws[kDrawGroup][2];
 #pragma unroll
     for (int ch = 0; ch < MAXC; ++ch) {
+      if (REGEN && kDrawGroup > 1 && ch % kDrawGroup == 0) {
+#pragma unroll
+        for (int k = 0; k < kDrawGroup; ++k) {
+          if (ch + k < MAXC) {
+            const uint64_t q = static_cast<uint64_t>(grow + (ch + k) * kChunk) >> 2;
+            draws[k][0] = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
+                                                   static_cast<uint32_t>(q >> 32), P.off0,
+                                                   P.off1),
+                                        P.rk);
+            draws[k][1] = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+                                                   static_cast<uint32_t>((q + 1) >> 32), P.off0,
+                                                   P.off1),
+                                        P.rk);
+          }
+        }
+      }
       float bt[8];   // this chunk's dbias terms
       if constexpr (TACC) {
         tmem_ld8(tacc + 24 * ch + 16, bt);
@@ -232,14 +255,18 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
         bool kept[8];   // the forward's keep decisions of these 8 elements
         if (REGEN) {
           // drawn again: element e is kept iff its Philox word >= thr
-          const uint64_t q = static_cast<uint64_t>(grow + ch * kChunk) >> 2;
-          const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
-                                                   static_cast<uint32_t>(q >> 32), P.off0, P.off1),
+          if (kDrawGroup == 1) {
+            const uint64_t q = static_cast<uint64_t>(grow + ch * kChunk) >> 2;
+            draws[0][0] = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
+                                                   static_cast<uint32_t>(q >> 32), P.off0,
+                                                   P.off1),
                                         P.rk);
-          const uint4 b = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
+            draws[0][1] = philox4x32_10(make_uint4(static_cast<uint32_t>(q + 1),
                                                    static_cast<uint32_t>((q + 1) >> 32), P.off0,
                                                    P.off1),
                                         P.rk);
+          }
+          const uint4 a = draws[ch % kDrawGroup][0], b = draws[ch % kDrawGroup][1];
           const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) kept[e] = u[e] >= P.thr;
