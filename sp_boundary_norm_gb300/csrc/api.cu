@@ -793,8 +793,9 @@ size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, s
   (void)norm;
   if (b <= 0 || s <= 0 || h < 8 || h % 8 != 0 || h > SP_MAX_HIDDEN || t < 1 || t > SP_MAX_RANKS)
     return 0;
-  // the largest grid over the variants (skip gradient or not, stored or
-  // regenerated mask): one workspace size serves every backward entry point
+  // the largest grid over the variants (skip gradient or not; stored mask,
+  // regenerated mask, or dYpre sent by bulk copies): one workspace size serves
+  // every backward entry point
   int grid = 0;
   for (int v = 0; v < 6; ++v) {   // skip gradient or not; stored, regenerated or bulk
     const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v >> 1) == 1, (v >> 1) == 2);
