@@ -32,8 +32,8 @@ def _built(lib):
     yield
 
 
-def _noalloc(w, fwd, gamma, dy, skip):
-    out = C.alloc_bwd(w, 1)
+def _noalloc(w, fwd, gamma, dy, skip, n_gather=1):
+    out = C.alloc_bwd(w, n_gather)
     C.sp.sp_norm_bwd_noalloc(dy, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], gamma, skip,
                              s=w.s, p=w.p, norm=w.norm, dresidual=out["dres"],
                              dgathered=out["dgat"], dgamma=out["dgamma"],
@@ -53,16 +53,18 @@ def _same(w, a, b):
         assert torch.equal(a[name].view(torch.int32), b[name].view(torch.int32)), name
 
 
-@pytest.mark.parametrize("norm,with_skip", [("layernorm", False), ("rmsnorm", True)])
-def test_noalloc_backward_matches_workspace_backward_twice(norm, with_skip):
+@pytest.mark.parametrize("norm,with_skip,n_gather", [("layernorm", False, 1),
+                                                    ("rmsnorm", True, 1),
+                                                    ("layernorm", False, 3)])
+def test_noalloc_backward_matches_workspace_backward_twice(norm, with_skip, n_gather):
     w = wl.Workload("na", t=4, b=1, s=2048, h=8192, norm=norm,
                     eps=1e-5 if norm == "layernorm" else 1e-6, draw_seed=51)
     inp = wl.forward_inputs(w, C.DEV)
     fwd = C.run_fwd(w, inp, n_gather=0)
     for call in range(2):   # two calls in a row, different upstream gradients
         b = wl.backward_inputs(w, C.DEV, seed=60 + call, with_skip=with_skip)
-        ref = C.run_bwd(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], n_gather=1)
-        got = _noalloc(w, fwd, inp["gamma"], b["dy"], b["dz_skip"])
+        ref = C.run_bwd(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], n_gather=n_gather)
+        got = _noalloc(w, fwd, inp["gamma"], b["dy"], b["dz_skip"], n_gather)
         torch.cuda.synchronize()
         C.sp.check_device_status(C.DEV)
         _same(w, got, ref)
