@@ -481,6 +481,8 @@ def test_70b_one_gathered_copy_per_rank():
     (dict(seqlens=(300, 17, 683), s=1000, t=3), 3),
     (dict(b=2, s=512, t=4), 2),              # gathered rows of two batch rows
     (dict(t=3, s=999, h=2056), 3),           # a row width that leaves chunks partial
+    (dict(s=64, h=16384), 2),                # the widest rows: 4 chunks, ring of 2
+    (dict(s=64, h=16384, skip=True), 3),     # ... with the skip gradient: ring of 1
 ])
 def test_backward_bulk_gathered_copies_equal_per_thread_stores(variant, n_gather):
     """With several gathered copies the backward writes each row's dYpre once
