@@ -47,7 +47,7 @@ def test_forward_full_size_every_element(name):
           f"{C.host_threads()} threads)")
 
 
-@pytest.mark.parametrize("name", ["bwd70b", "bwd70b_rms", "ragged"])
+@pytest.mark.parametrize("name", ["bwd70b", "bwd70b_rms", "ragged", "trace4k"])
 def test_backward_full_size_every_element(name):
     w = wl.WORKLOADS[name]
     inp = wl.forward_inputs(w, C.DEV)
@@ -87,27 +87,30 @@ def test_mask_free_backward_full_size_every_element(name):
     print(f"\nfull-size mask-free backward {name}: {tot} ({time.perf_counter() - t0:.1f} s)")
 
 
-def test_rs_norm_bwd_full_size_every_element():
-    """The backward entered through g at the 70B shape: dY is the float32
+@pytest.mark.parametrize("name", ["bwd70b", "ragged"])
+def test_rs_norm_bwd_full_size_every_element(name):
+    """The backward entered through g at full size (the 70B shape, and the
+    packed workload with its uneven shards): dY is the float32
     rank-ascending sum of the t ranks' partial gradients of the gathered
     input (the reduce-scatter that is the gradient of g, "第 7 课" §3.B),
     fused into the norm backward; every element against the oracle."""
-    w = wl.WORKLOADS["bwd70b"]
+    w = wl.WORKLOADS[name]
     inp = wl.forward_inputs(w, C.DEV)
     fwd = C.run_fwd(w, inp, n_gather=0)
     gen = wl.make_generator(97, C.DEV)
     parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=C.DEV) * 0.35).to(torch.bfloat16)
              for _ in range(w.t)]
     out = C.alloc_bwd(w, 1)
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
     C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
-                        None, p=w.p, norm=w.norm, dresidual=out["dres"], dgathered=out["dgat"],
-                        dgamma=out["dgamma"], dbeta=out["dbeta"], dbias=out["dbias"],
-                        workspace=out["ws"])
+                        None, p=w.p, norm=w.norm, cu_seqlens=cu, dresidual=out["dres"],
+                        dgathered=out["dgat"], dgamma=out["dgamma"], dbeta=out["dbeta"],
+                        dbias=out["dbias"], workspace=out["ws"])
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     t0 = time.perf_counter()
     tot = C.full_bwd_check(w, fwd, inp["gamma"], None, None, out, dy_partials=parts)
-    print(f"\nfull-size backward through g: {tot} ({time.perf_counter() - t0:.1f} s)")
+    print(f"\nfull-size backward through g, {name}: {tot} ({time.perf_counter() - t0:.1f} s)")
 
 
 def test_70b_one_gathered_copy_per_rank_every_element():
