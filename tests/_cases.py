@@ -80,6 +80,25 @@ def run_bwd(w, fwd_out, gamma, dy, dz_skip=None, n_gather=None, out=None, cu_seq
     return out
 
 
+def run_unfused(w, inp, n_gather=1):
+    """The boundary as three calls: reduce-scatter (bf16 shards), the norm on
+    the shards, all-gather of the shards' O.  Returns (y, o, out)."""
+    sizes = w.shard_sizes()
+    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=DEV)
+    y = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+    out = alloc_fwd(w, n_gather)
+    o = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(DEV) if w.ragged else None
+    sp.sp_reduce_scatter_seq(inp["partials"], y, cu_seqlens=cu)
+    sp.sp_shard_norm_fwd(y, inp["residual"], inp["bias"], inp["gamma"], inp["beta"], s=w.s,
+                         eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                         cu_seqlens=cu, z_out=out["z"], mask_out=out["mask"],
+                         mean_out=out["mean"], rstd_out=out["rstd"], o_shards=o)
+    if n_gather:
+        sp.sp_allgather_seq(o, out["gathered"], s=w.s, cu_seqlens=cu)
+    return y, o, out
+
+
 def token_shard(w, g):
     """(shard k, local row) of global token g for b == 1 or dense b > 1."""
     bi, si = divmod(int(g), w.s)
@@ -347,4 +366,51 @@ def full_bwd_check(w, fwd_out, gamma, dy, dz_skip, out, dy_partials=None):
         bad = compare.colsum_mismatch(got, acc, np.sqrt(sq))
         assert not bad.any(), f"{name}: {bad.sum()} channels off"
     tot["elements"] = n
+    return tot
+
+
+def full_unfused_fwd_check(w, inp, y, o, out):
+    """Every token of the unfused boundary: the reduce-scatter's bf16 shard
+    rows equal the oracle's rank-ascending float32 sum rounded to bf16 (bit
+    for bit); the shard step's Z and mask (bit for bit), statistics and O
+    (bf16 bar) equal the oracle's token-wise forward of those rows; every
+    gathered copy holds the shards' O bit for bit.  Returns the counts."""
+    from oracle import bf16 as obf
+    from oracle import collectives as oc
+    h, T = w.h, w.tokens
+    parts = [_full_bits(P, h) for P in inp["partials"]]
+    R = _bits_rows(inp["residual"], h)
+    Y = _bits_rows(y, h)
+    Z = _bits_rows(out["z"], h)
+    M = _u8_rows(out["mask"], h)
+    RS = _vec_rows(out["rstd"])
+    MU = _vec_rows(out["mean"]) if w.norm == "layernorm" else None
+    O = _bits_rows(o, h)
+    G = [_full_bits(g, h) for g in out["gathered"]]
+    bias, gamma, beta = f32(inp["bias"]), f32(inp["gamma"]), f32(inp["beta"])
+
+    def chunk(lo):
+        hi = min(T, lo + CHUNK)
+        shards, _ = oc.reduce_scatter_seq([_val(P[lo:hi])[None] for P in parts])
+        y16 = obf.bf16_round(np.concatenate([np.asarray(x).reshape(-1, h) for x in shards]))
+        ref = ob.forward_rows(y16[None], _val(R[lo:hi]), np.arange(lo, hi, dtype=np.int64),
+                              bias, gamma, beta, eps=w.eps, p=w.p, seed=w.seed,
+                              offset=w.offset, norm=w.norm)
+        return {"y_bad": int((Y[lo:hi] != compare.bf16_bits(y16)).sum()),
+                "z_bad": int((Z[lo:hi] != compare.bf16_bits(ref["z"])).sum()),
+                "mask_bad": int((M[lo:hi] != ref["mask"]).sum()),
+                "rstd_bad": int(compare.f32_rel_mismatch(RS[lo:hi], ref["rstd"]).sum()),
+                "mean_bad": 0 if MU is None else
+                int(compare.f32_rel_mismatch(MU[lo:hi], ref["mean"]).sum()),
+                "o_bad": int(compare.bf16_mismatch(O[lo:hi], ref["out_exact"],
+                                                   ref["out_magnitude"]).sum()),
+                "o_floor_only": int(compare.bf16_floor_only(O[lo:hi], ref["out_exact"],
+                                                            ref["out_magnitude"]).sum()),
+                "gathered_bad": sum(int((g[lo:hi] != O[lo:hi]).sum()) for g in G)}
+
+    tot = _add_counts(_pool_map(chunk, T))
+    for key in ("y_bad", "z_bad", "mask_bad", "rstd_bad", "mean_bad", "o_bad", "gathered_bad"):
+        assert tot[key] == 0, tot
+    assert tot["o_floor_only"] <= compare.floor_only_bound(T * h), tot
+    tot["elements"] = T * h
     return tot

@@ -131,3 +131,19 @@ def test_70b_one_gathered_copy_per_rank_every_element():
     g = C.full_bwd_check(w, fwd, inp["gamma"], dy, None, out)
     print(f"\nfull-size n_gather={w.t}: forward {f}, backward {g} "
           f"({time.perf_counter() - t0:.1f} s)")
+
+
+@pytest.mark.parametrize("name", ["70b", "ragged"])
+def test_unfused_pipeline_full_size_every_element(name):
+    """The unfused boundary (reduce-scatter, norm on the shards, all-gather:
+    the ablation of the fusion) at full size, every element against the
+    oracle: the bf16 shards of the reduce-scatter, Z, mask, statistics, O and
+    the gathered copy."""
+    w = wl.WORKLOADS[name]
+    inp = wl.forward_inputs(w, C.DEV)
+    y, o, out = C.run_unfused(w, inp)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    t0 = time.perf_counter()
+    tot = C.full_unfused_fwd_check(w, inp, y, o, out)
+    print(f"\nfull-size unfused forward {name}: {tot} ({time.perf_counter() - t0:.1f} s)")

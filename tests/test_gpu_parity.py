@@ -628,28 +628,12 @@ def test_device_philox_matches_oracle():
 
 # ----------------------------------------------- unfused boundary (ablation)
 
-def _run_unfused(w, inp, n_gather=1):
-    sizes = w.shard_sizes()
-    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=C.DEV)
-    y = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
-    out = C.alloc_fwd(w, n_gather)
-    o = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
-    C.sp.sp_reduce_scatter_seq(inp["partials"], y)
-    C.sp.sp_shard_norm_fwd(y, inp["residual"], inp["bias"], inp["gamma"], inp["beta"], s=w.s,
-                           eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
-                           z_out=out["z"], mask_out=out["mask"], mean_out=out["mean"],
-                           rstd_out=out["rstd"], o_shards=o)
-    if n_gather:
-        C.sp.sp_allgather_seq(o, out["gathered"], s=w.s)
-    return y, o, out
-
-
 @pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(t=3, s=48),
                                      dict(b=2, s=40, t=4), dict(h=5120, s=32), dict(p=0.0)])
 def test_unfused_pipeline_matches_oracle(variant):
     w = wl.Workload("uf", t=2, b=1, s=64, h=512, draw_seed=61).with_(**variant)
     inp = wl.forward_inputs(w, C.DEV)
-    y, o, out = _run_unfused(w, inp)
+    y, o, out = C.run_unfused(w, inp)
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     ref = ob.unfused_fwd([C.f32(x) for x in inp["partials"]], [C.f32(x) for x in inp["residual"]],
@@ -680,7 +664,7 @@ def test_unfused_pipeline_70b_sampled():
     from oracle import collectives as oc
     w = wl.WORKLOADS["70b"]
     inp = wl.forward_inputs(w, C.DEV)
-    y, o, out = _run_unfused(w, inp)
+    y, o, out = C.run_unfused(w, inp)
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     tokens = C.sample_tokens(w, 48)
@@ -712,7 +696,7 @@ def test_unfused_pipeline_70b_sampled():
 def test_unfused_mask_equals_fused_mask():
     w = wl.Workload("ufm", t=4, b=1, s=128, h=1024, draw_seed=62)
     inp = wl.forward_inputs(w, C.DEV)
-    _, _, un = _run_unfused(w, inp)
+    _, _, un = C.run_unfused(w, inp)
     fu = C.run_fwd(w, inp)
     torch.cuda.synchronize()
     for a, b in zip(un["mask"], fu["mask"]):
