@@ -153,9 +153,10 @@ def test_forward_row_split_over_a_cta_pair(fwd_split, variant, threads):
     _full_fwd_compare(w, inp, out)
 
 
-def test_forward_row_split_ragged_and_70b_sampled(fwd_split):
-    """The CTA-pair forward on packed uneven shards (full compare) and on the
-    70B shape (sampled rows and the drop rate)."""
+def test_forward_row_split_ragged_and_70b_every_element(fwd_split):
+    """The CTA-pair forward on packed uneven shards and on the 70B shape,
+    every element against the oracle (the 70B check through the chunked,
+    thread-pooled oracle), and the drop rate."""
     fwd_split(2, 128)
     lengths = (33, 64, 7, 1, 90, 12)
     w = wl.Workload("rp", t=5, b=1, s=sum(lengths), h=512, seqlens=lengths, draw_seed=142)
@@ -173,7 +174,7 @@ def test_forward_row_split_ragged_and_70b_sampled(fwd_split):
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     assert C.sp.sp_debug_last_shape(0)["cluster"] == 2
-    C.check_fwd_rows(w, inp, out, C.sample_tokens(w, 64))
+    C.full_fwd_check(w, inp, out)
     kept = sum(int(m.sum()) for m in out["mask"])
     n = w.tokens * w.h
     assert abs((1 - kept / n) - w.p) < 5 * np.sqrt(w.p * (1 - w.p) / n)
