@@ -28,7 +28,6 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
   __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
   __shared__ __align__(8) uint64_t xbar[2];   // CL > 1: the partner's row sums arrived
   __shared__ __align__(8) float2 xpub[2];     // CL > 1: this CTA's row sums, published
-  __shared__ int abort_flag;   // nonzero once any thread of the block gave up a wait
   constexpr int kWarps = NTHR / 32;   // compute warps; warp kWarps issues the copies
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -55,7 +54,6 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       mbar_init(&xbar[0], 1);
       mbar_init(&xbar[1], 1);
     }
-    abort_flag = 0;
     mbar_fence_init();
   }
   if (CL > 1)
@@ -86,20 +84,23 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
   // right after reading it, so a stage refills while the previous chunk is
   // still being computed): it arms the stage's full barrier with the item's
   // byte count and issues one bulk copy per stream.
-  // Giving up is well defined: a thread whose wait runs out raises the
-  // block's abort flag; from then on no thread waits on, reads or releases a
-  // stage, the producer issues nothing more, and before the block ends it
-  // waits (bounded) for exactly the copies it did issue, so no copy lands in
-  // shared memory after the block has gone.  The call then reports
-  // SP_ERR_TIMEOUT and its outputs are undefined.
-  volatile int* const abort_v = &abort_flag;
+  // Giving up is well defined: a compute thread whose wait runs out stops
+  // waiting, and its warp stops releasing stages, from then on.  The
+  // producer issues an item only after every compute warp has released the
+  // stage's previous item, which a warp does only once that item's copies
+  // have landed, so no stage is refilled while its phase has bytes pending;
+  // when the producer's own wait runs out it issues nothing more, and before
+  // the block ends it waits (bounded) for exactly the copies it did issue,
+  // so no copy lands in shared memory after the block has gone.  A failure
+  // costs at most two wait limits; the call then reports SP_ERR_TIMEOUT and
+  // its outputs are undefined.
   bool timed_out = false;   // this thread's own wait ran out
   if (tid >= NTHR) {
     if (lane == 0) {
       RowWalk pf;
       pf.init(P.map, r0);
       int64_t item = 0;   // items attempted so far, in order; all but a withheld one issued
-      for (int64_t ri = 0; ri < nrows && *abort_v == 0; ++ri) {
+      for (int64_t ri = 0; ri < nrows; ++ri) {
         if (ri > 0) pf.next(P.map, step);
         const int64_t goff = pf.row * h + coff, roff = pf.local * h + coff;
         const int kk = pf.k;
@@ -107,16 +108,9 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
         for (; ch < nchunk; ++ch, ++item) {
           const int s = static_cast<int>(item % STAGES);
           const int64_t use = item / STAGES;
-          if (use > 0) {
-            const int r = mbar_wait_or_abort(&bar_empty[s], static_cast<uint32_t>((use - 1) & 1),
-                                             abort_v);
-            if (r != kWaitDone) {
-              if (r == kWaitTimedOut) {
-                timed_out = true;
-                *abort_v = 1;
-              }
-              break;
-            }
+          if (use > 0 && !mbar_wait(&bar_empty[s], static_cast<uint32_t>((use - 1) & 1))) {
+            timed_out = true;
+            break;
           }
           if (P.withhold != 0 && blockIdx.x == 0 && item == 0) continue;   // test hook
           const int cc = ch * kChunk;
@@ -154,7 +148,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
 
   RowWalk cur;
   cur.init(P.map, r0);
-  bool gave_up = false;   // this thread stopped waiting (its wait ran out, or the block aborted)
+  bool gave_up = false;   // this thread's wait ran out: it waits and releases no more
   int slot_sel = 0;
   const float inv_h = 1.f / static_cast<float>(h);
 
@@ -178,15 +172,11 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
       }
       float2 other = make_float2(0.f, 0.f);
       if (lane == 0 && !gave_up) {
-        const int r = mbar_wait_cluster_or_abort(&xbar[slot], par, abort_v);
-        if (r == kWaitDone) {
+        if (mbar_wait_cluster(&xbar[slot], par)) {
           other = ld_cluster_f2(cluster_map(&xpub[slot], peer));
         } else {
           gave_up = true;
-          if (r == kWaitTimedOut) {
-            timed_out = true;
-            *abort_v = 1;
-          }
+          timed_out = true;
         }
       }
       other.x = __shfl_sync(0xFFFFFFFFu, other.x, 0);
@@ -210,25 +200,20 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     for (int ch = 0; ch < nchunk; ++ch) {
       const int64_t item = ri * nchunk + ch;
       const int stage = static_cast<int>(item % STAGES);
-      bool have = false;   // the item has landed and this thread may read it
-      if (!gave_up) {
-        const int r = mbar_wait_or_abort(&bar_full[stage],
-                                         static_cast<uint32_t>((item / STAGES) & 1), abort_v);
-        have = r == kWaitDone;
-        if (!have) {
-          gave_up = true;
-          if (r == kWaitTimedOut) {
-            timed_out = true;
-            *abort_v = 1;
-          }
-        }
+      // the item has landed (after a give-up the thread reads whatever the
+      // stage holds: the outputs are undefined then, and it releases nothing)
+      bool have = !gave_up;
+      if (have && !mbar_wait(&bar_full[stage], static_cast<uint32_t>((item / STAGES) & 1))) {
+        have = false;
+        gave_up = true;
+        timed_out = true;
       }
       const int cc = ch * kChunk;
       // g*: float32 sum of the t partials, ranks in ascending order
       // ((P_0 + P_1) + P_2) + ...; each add widens its bf16 operand exactly
-      float y[8] = {};
+      float y[8];
       uint4 rv = make_uint4(0, 0, 0, 0);
-      if (have && cc + c0 < hl) {
+      if (cc + c0 < hl) {
         const uint8_t* slot = smem + stage * stage_bytes + tid * 16;
         unpack8(lds16(slot), y);
         if (!SHARD) {

@@ -291,14 +291,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t byte
                : "memory");
 }
 
+// A thread whose phase is still pending is suspended by the hardware for up
+// to this long (or until the phase completes) before try_wait returns false,
+// so a waiting thread takes no issue slots from the warps that compute.
+constexpr uint32_t kTryWaitSuspendNs = 1000000;   // 1 ms
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(b)), "r"(parity)
+      : "r"(smem_addr(b)), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -311,25 +316,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
   while (!mbar_try_wait(b, parity))
     if (global_ns() - t0 > kWaitLimitNs) return false;
   return true;
-}
-
-// Outcome of a wait that can also be called off by another thread of the
-// block: the phase completed, this thread's own wait ran out (kWaitLimitNs),
-// or another thread had given up first and raised the block's abort flag.
-enum WaitResult { kWaitDone = 0, kWaitTimedOut = 1, kWaitAborted = 2 };
-
-// mbar_wait that also returns as soon as *abort_flag is nonzero.  The flag is
-// read only while the phase is still pending, so a wait that succeeds at once
-// costs the same as mbar_wait.
-__device__ __forceinline__ int mbar_wait_or_abort(uint64_t* b, uint32_t parity,
-                                                  const volatile int* abort_flag) {
-  if (mbar_try_wait(b, parity)) return kWaitDone;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(b, parity)) {
-    if (*abort_flag != 0) return kWaitAborted;
-    if (global_ns() - t0 > kWaitLimitNs) return kWaitTimedOut;
-  }
-  return kWaitDone;
 }
 
 // One contiguous global -> shared copy (16-byte aligned ends, a multiple of
@@ -404,24 +390,21 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* b, uint32_t pari
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(b)), "r"(parity)
+      : "r"(smem_addr(b)), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
 
-// Bounded and abortable like mbar_wait_or_abort.
-__device__ __forceinline__ int mbar_wait_cluster_or_abort(uint64_t* b, uint32_t parity,
-                                                          const volatile int* abort_flag) {
-  if (mbar_try_wait_cluster(b, parity)) return kWaitDone;
+// Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity) {
+  if (mbar_try_wait_cluster(b, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait_cluster(b, parity)) {
-    if (*abort_flag != 0) return kWaitAborted;
-    if (global_ns() - t0 > kWaitLimitNs) return kWaitTimedOut;
-  }
-  return kWaitDone;
+  while (!mbar_try_wait_cluster(b, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 
 __device__ __forceinline__ float2 ld_cluster_f2(uint32_t cluster_addr) {
