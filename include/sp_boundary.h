@@ -318,8 +318,8 @@ int32_t sp_abi_version(void);
  * disarms itself.  SP_OK disarms it.  SP_ERR_TIMEOUT is the exception when
  * the next call is sp_rs_norm_fwd or sp_shard_norm_fwd: that call launches
  * normally except that block 0's copy producer never stages the block's
- * first chunk, so the block's bounded waits run out (about a second) and the
- * call's dev_status reads SP_ERR_TIMEOUT; that block's rows hold undefined
+ * first chunk, so the block's bounded waits run out (one to two seconds) and
+ * the call's dev_status reads SP_ERR_TIMEOUT; that block's rows hold undefined
  * values.  It shows the waits are bounded, without faulting or hanging.
  */
 sp_status_t sp_debug_inject(sp_status_t code);
