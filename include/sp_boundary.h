@@ -27,6 +27,11 @@
  *  - Calls are asynchronous: they validate on the host, enqueue on `stream`
  *    (a cudaStream_t; NULL = the legacy default stream) and return.  A host
  *    validation failure returns an error code before anything is enqueued.
+ *    Kernels are launched with programmatic stream serialisation: a call's
+ *    kernel may start on the SMs while the kernel before it on `stream` is
+ *    completing, but touches no global memory before that kernel's writes
+ *    are visible, so stream order holds as for plain launches (also when the
+ *    calls are captured into a CUDA graph).
  *    Device-side checks (cu_seqlens contents) write a nonzero sp_status_t into
  *    `dev_status` (a caller-owned device int32, may be NULL) and never clear it.
  *  - Outputs must not overlap inputs or each other (checked on the host).

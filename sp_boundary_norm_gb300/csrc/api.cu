@@ -492,28 +492,36 @@ cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStre
   cudaError_t e = ensure_smem_attr(fn, ls.smem);
   if (e != cudaSuccess) return e;
   void* args[] = {params};
-  if (ls.cluster > 1) {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = ls.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ls.grid);
-    cfg.blockDim = dim3(ls.threads);
-    cfg.dynamicSmemBytes = ls.smem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-  } else {
-    e = cudaLaunchKernel(fn, dim3(ls.grid), dim3(ls.threads), args, ls.smem, st);
-  }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_pdl(fn, dim3(ls.grid), dim3(ls.threads), ls.smem, args, st, ls.cluster);
 }
 
 }  // namespace
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, void** args,
+                       cudaStream_t st, int cluster) {
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 sp_status_t record_error(sp_status_t code, const char* message) {
   return fail(code, "%s", message);

@@ -34,6 +34,7 @@ constexpr int kReduceWarps = 8;
 
 __global__ void __launch_bounds__(32 * kReduceWarps) param_reduce_kernel(const ParamReduceParams P) {
   __shared__ float part[kReduceWarps][32];
+  pdl_wait();
   const int q = blockIdx.y;
   float* out = P.out[q];
   if (out == nullptr) return;   // uniform per block
@@ -79,8 +80,9 @@ const void* bwd_kernel(int threads, int maxc, int ring) {
 
 cudaError_t launch_param_reduce(const ParamReduceParams& p, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>((p.h + 31) / 32), 3);
-  param_reduce_kernel<<<grid, 32 * kReduceWarps, 0, st>>>(p);
-  return cudaGetLastError();
+  void* args[] = {const_cast<ParamReduceParams*>(&p)};
+  return launch_pdl(reinterpret_cast<const void*>(&param_reduce_kernel), grid,
+                    dim3(32 * kReduceWarps), 0, args, st);
 }
 
 }  // namespace spb

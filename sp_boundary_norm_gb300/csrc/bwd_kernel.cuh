@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x;
+  pdl_wait();   // before tensor memory is taken, too
   // tensor memory: allocated by warp 0 before anything can diverge
   uint32_t tacc = 0;   // this thread's lane, first of its columns
   if constexpr (TACC) {

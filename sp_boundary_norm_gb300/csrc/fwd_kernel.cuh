@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     cluster_sync_all();   // the partner's mbarriers are initialised too
   else
     __syncthreads();
+  pdl_wait();
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
   // this block's rows (a cluster's: both CTAs walk the same rows): every G-th

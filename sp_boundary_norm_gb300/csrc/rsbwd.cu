@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(NTHR, 1) rs_norm_bwd_kernel(const BwdParams P)
   for (int ch = 0; ch < MAXC; ++ch)
     if (ch < nchunk && ch * kChunk + c0 < h) valid |= 1u << ch;
 
+  pdl_wait();
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
   // this block's rows: a contiguous range

@@ -15,6 +15,7 @@ constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
 __global__ void __launch_bounds__(kCopyThreads) allgather_kernel(const CopyParams P) {
+  pdl_wait();
   if (blockIdx.x == 0 && threadIdx.x < 32)
     check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
   const int64_t h = P.map.h;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(kCopyThreads) allgather_kernel(const CopyParam
 template <int TT>
 __global__ void __launch_bounds__(kCopyThreads) reduce_scatter_kernel(const CopyParams P,
                                                                       int t) {
+  pdl_wait();
   if (blockIdx.x == 0 && threadIdx.x < 32)
     check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
   const int64_t h = P.map.h;
@@ -108,16 +110,16 @@ static int copy_grid(int64_t rows) {
 }
 
 cudaError_t launch_allgather(const CopyParams& p, cudaStream_t st) {
-  allgather_kernel<<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  void* args[] = {const_cast<CopyParams*>(&p)};
+  return launch_pdl(reinterpret_cast<const void*>(&allgather_kernel), dim3(copy_grid(p.rows)),
+                    dim3(kCopyThreads), 0, args, st);
 }
 
 cudaError_t launch_reduce_scatter(const CopyParams& p, int t, cudaStream_t st) {
-  if (t == 8)
-    reduce_scatter_kernel<8><<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p, t);
-  else
-    reduce_scatter_kernel<0><<<copy_grid(p.rows), kCopyThreads, 0, st>>>(p, t);
-  return cudaGetLastError();
+  void* args[] = {const_cast<CopyParams*>(&p), &t};
+  const void* fn = t == 8 ? reinterpret_cast<const void*>(&reduce_scatter_kernel<8>)
+                          : reinterpret_cast<const void*>(&reduce_scatter_kernel<0>);
+  return launch_pdl(fn, dim3(copy_grid(p.rows)), dim3(kCopyThreads), 0, args, st);
 }
 
 cudaError_t launch_debug_philox(const uint32_t* in, uint32_t* out, int64_t n, cudaStream_t st) {

@@ -256,6 +256,17 @@ __device__ __forceinline__ void st8_stream(void* p, uint2 v) {
   __stcs(reinterpret_cast<uint2*>(p), v);
 }
 
+// ------------------------------------------ programmatic dependent launch --
+// Every kernel of the library is launched with programmatic stream
+// serialisation and never signals its dependents early, so the next kernel's
+// blocks are placed as soon as every block of this one has exited, without
+// the gap of a plain launch.  pdl_wait() returns once the previous kernel on
+// the stream has completed and its memory operations are visible (at once for
+// a plain launch); each kernel calls it, in every thread, before its first
+// global memory access.  (Signalling earlier, so that the next kernel's
+// blocks wait beside this kernel's last ones, measured slower.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------- bulk copies and mbarriers --
 // The forward stages its inputs with bulk global -> shared copies issued by
 // one producer warp and completed on mbarriers (transaction counts), the

@@ -140,6 +140,15 @@ struct LaunchShape {
 
 int device_sm_count();
 
+// Launches kernel `fn` (one parameter-struct argument per entry of `args`)
+// with programmatic stream serialisation, and a cluster dimension of
+// `cluster` CTAs when above 1: its blocks are placed as soon as every block
+// of the previous kernel on the stream has exited, and every kernel of the
+// library waits for that kernel's memory operations (pdl_wait) before its
+// first global memory access.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, void** args,
+                       cudaStream_t st, int cluster = 1);
+
 // Sets the thread's sp_last_error() text; returns `code`.
 sp_status_t record_error(sp_status_t code, const char* message);
 

@@ -1,0 +1,170 @@
+"""Stream order across the library's calls.
+
+Every kernel of the library is launched with programmatic stream
+serialisation: its blocks may be placed on the SMs while the previous kernel
+on the stream is still running, and each waits for that kernel to complete
+before it touches global memory.  These tests run chains of calls in which
+every call reads what the call before it wrote, and writes buffers that the
+call before it read (two buffer sets, alternating), and require the chain to
+give bit for bit what the same chain gives with the device synchronised after
+every call -- back to back on one stream and replayed as one CUDA graph.
+Every kernel is deterministic, so any read of a buffer before its producer
+finished, or any write before its last reader finished, shows as a changed
+bit."""
+import pytest
+import torch
+
+from sp_boundary_norm_gb300 import binding as sp
+from sp_boundary_norm_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("_cases")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+
+STEPS = 4
+
+
+def _alloc_set(w, dev):
+    """One buffer set: everything one step of the chain writes."""
+    sizes = w.shard_sizes()
+    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+    shard = lambda dt: [e((w.b, n, w.h), dt) for n in sizes]
+    stats = lambda: [e((w.b, n), torch.float32) for n in sizes]
+    full = lambda k: [e((w.b, w.s, w.h), torch.bfloat16) for _ in range(k)]
+    vec = lambda: e((w.h,), torch.float32)
+    st = {
+        # fused forward
+        "z": shard(torch.bfloat16), "mask": shard(torch.uint8), "mean": stats(),
+        "rstd": stats(), "g": full(w.t),
+        # backward from the shards (stored mask) and its parameter gradients
+        "d": shard(torch.bfloat16), "dg": full(1), "dgamma": vec(), "dbeta": vec(),
+        "dbias": vec(),
+        # backward entered through g (the t partial gradients reduce-scattered)
+        "d2": shard(torch.bfloat16), "dg2": full(1), "dgamma2": vec(), "dbeta2": vec(),
+        "dbias2": vec(),
+        # the unfused forward: reduce-scatter, norm on the shards, all-gather
+        "y": shard(torch.bfloat16), "z2": shard(torch.bfloat16), "mask2": shard(torch.uint8),
+        "mean2": stats(), "rstd2": stats(), "o2": shard(torch.bfloat16), "g2": full(1),
+    }
+    if w.norm != "layernorm":   # RMSNorm has no mean and no beta
+        for key in ("mean", "mean2", "dbeta", "dbeta2"):
+            del st[key]
+    return st
+
+
+def _tensors(st):
+    for v in st.values():
+        if isinstance(v, list):
+            yield from v
+        else:
+            yield v
+
+
+def _poison(sets):
+    for st in sets:
+        for x in _tensors(st):
+            if x.dtype == torch.uint8:
+                x.fill_(0xA5)
+            else:
+                x.fill_(float("nan"))
+
+
+def _chain(w, inp, dy, cu, sets, ws, sync):
+    """STEPS steps; step i reads set (i - 1) % 2 (the inputs for i = 0) and
+    writes set i % 2.  Per step: fused forward -> backward from the shards
+    (+ parameter reduce) -> backward through g (+ parameter reduce) ->
+    reduce-scatter -> shard norm -> all-gather."""
+    after = (lambda: torch.cuda.synchronize()) if sync else (lambda: None)
+    prev = {"g": inp["partials"], "z2": inp["residual"], "d2": dy}
+    for i in range(STEPS):
+        cur = sets[i % 2]
+        sp.sp_rs_norm_fwd(prev["g"], prev["z2"], inp["bias"], inp["gamma"], inp["beta"],
+                          eps=w.eps, p=w.p, seed=w.seed, offset=w.offset + i, norm=w.norm,
+                          cu_seqlens=cu, z_out=cur["z"], mask_out=cur["mask"],
+                          mean_out=cur.get("mean"), rstd_out=cur["rstd"], gathered=cur["g"])
+        after()
+        sp.sp_norm_bwd(prev["d2"], cur["z"], cur["mask"], cur.get("mean"), cur["rstd"],
+                       inp["gamma"], None, s=w.s, p=w.p, norm=w.norm, cu_seqlens=cu,
+                       dresidual=cur["d"], dgathered=cur["dg"], dgamma=cur["dgamma"],
+                       dbeta=cur.get("dbeta"), dbias=cur["dbias"], workspace=ws)
+        after()
+        sp.sp_rs_norm_bwd(cur["g"], cur["z"], cur["mask"], cur.get("mean"), cur["rstd"],
+                          inp["gamma"], None, p=w.p, norm=w.norm, cu_seqlens=cu,
+                          dresidual=cur["d2"], dgathered=cur["dg2"], dgamma=cur["dgamma2"],
+                          dbeta=cur.get("dbeta2"), dbias=cur["dbias2"],
+                          workspace=ws)
+        after()
+        sp.sp_reduce_scatter_seq(cur["g"], cur["y"], cu_seqlens=cu)
+        after()
+        sp.sp_shard_norm_fwd(cur["y"], cur["d"], inp["bias"], inp["gamma"], inp["beta"], s=w.s,
+                             eps=w.eps, p=w.p, seed=w.seed, offset=w.offset + 100 + i,
+                             norm=w.norm, cu_seqlens=cu, z_out=cur["z2"],
+                             mask_out=cur["mask2"], mean_out=cur.get("mean2"),
+                             rstd_out=cur["rstd2"], o_shards=cur["o2"])
+        after()
+        sp.sp_allgather_seq(cur["o2"], cur["g2"], s=w.s, cu_seqlens=cu)
+        after()
+        prev = cur
+
+
+def _snapshot(sets):
+    return [[x.clone() for x in _tensors(st)] for st in sets]
+
+
+def _same(a, b):
+    for sa, sb in zip(a, b):
+        for x, y in zip(sa, sb):
+            if x.dtype == torch.float32:
+                x, y = x.view(torch.int32), y.view(torch.int32)
+            if not torch.equal(x, y):
+                return False
+    return True
+
+
+@pytest.mark.parametrize("variant", [
+    dict(t=4, b=1, s=2048, h=4096),
+    dict(t=8, b=2, s=1024, h=8192, norm="rmsnorm", eps=1e-6),
+    dict(t=4, b=1, s=2048, h=5120, seqlens=(700, 1, 1200, 147)),
+])
+def test_dependent_calls_back_to_back_and_in_a_graph_equal_synchronised_calls(variant):
+    w = wl.Workload("chain", draw_seed=515, p=0.1, **variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+    sets = [_alloc_set(w, C.DEV), _alloc_set(w, C.DEV)]
+    ws = torch.empty(max(16, sp.sp_norm_bwd_workspace_bytes(w.b, w.s, w.h, w.t, w.norm)),
+                     dtype=torch.uint8, device=C.DEV)
+
+    _poison(sets)
+    _chain(w, inp, dy, cu, sets, ws, sync=True)
+    torch.cuda.synchronize()
+    sp.check_device_status(C.DEV)
+    ref = _snapshot(sets)
+    for st in sets:   # every output written and finite
+        for x in _tensors(st):
+            if x.dtype != torch.uint8:
+                assert torch.isfinite(x.float()).all()
+
+    for rep in range(3):
+        _poison(sets)
+        _chain(w, inp, dy, cu, sets, ws, sync=False)
+        torch.cuda.synchronize()
+        sp.check_device_status(C.DEV)
+        assert _same(ref, _snapshot(sets)), f"back to back, repetition {rep}"
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _chain(w, inp, dy, cu, sets, ws, sync=False)
+    for rep in range(3):
+        _poison(sets)
+        g.replay()
+        torch.cuda.synchronize()
+        sp.check_device_status(C.DEV)
+        assert _same(ref, _snapshot(sets)), f"graph replay {rep}"
