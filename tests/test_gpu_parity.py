@@ -25,24 +25,7 @@ def _built(lib):
     yield
 
 
-def _full_fwd_compare(w, inp, out):
-    ref = ob.rs_norm_fwd([C.f32(x) for x in inp["partials"]], [C.f32(x) for x in inp["residual"]],
-                         C.f32(inp["bias"]), C.f32(inp["gamma"]), C.f32(inp["beta"]), eps=w.eps,
-                         p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
-                         n_gather=len(out["gathered"]))
-    for k in range(w.t):
-        assert np.array_equal(compare.bf16_bits(out["z"][k]), compare.bf16_bits(ref["z"][k])), k
-        assert np.array_equal(out["mask"][k].cpu().numpy(), ref["mask"][k]), k
-        assert not compare.f32_rel_mismatch(out["rstd"][k].cpu().numpy(), ref["rstd"][k]).any()
-        if w.norm == "layernorm":
-            assert not compare.f32_rel_mismatch(out["mean"][k].cpu().numpy(), ref["mean"][k]).any()
-    out_exact = np.concatenate(ref["out_exact"], axis=1)
-    mag = np.concatenate([ob._norm_rows(z.reshape(-1, w.h).astype(np.float64), C.f32(inp["gamma"]),
-                                        C.f32(inp["beta"]), w.eps, w.norm)[3].reshape(z.shape)
-                          for z in ref["z"]], axis=1)
-    for j, g in enumerate(out["gathered"]):
-        C.assert_bf16(compare.bf16_bits(g), out_exact, mag, f"gathered[{j}]")
-    return ref
+_full_fwd_compare = C.fwd_compare_all
 
 
 @pytest.mark.parametrize("name", ["tiny", "trace4k"])
@@ -848,43 +831,7 @@ def test_mask_free_backward_70b_sampled():
 
 # ------------------------------------------ backward entered through g
 
-def _rs_bwd_check(w, fwd, inp, parts, skip, out, tokens=None):
-    """dResidual / dYpre rows and parameter sums against the oracle, with dY
-    the float32 rank-ascending sum of the partial gradients on each shard."""
-    from oracle import collectives as coll
-    h = w.h
-    flat = [C.f32(x) for x in parts]
-    dy_shards, _ = coll.reduce_scatter_seq(flat)
-    offs = [(k * w.s) // w.t for k in range(w.t + 1)]
-    g = C.f32(inp["gamma"])
-    acc = {n: np.zeros(h) for n in ("dgamma", "dbeta", "dbias")}
-    sq = {n: np.zeros(h) for n in acc}
-    scale = float(ob.dropout_scale(w.p))
-    for k in range(w.t):
-        n = w.b * (offs[k + 1] - offs[k])
-        if n == 0:
-            continue
-        rows = lambda x: x[k].reshape(-1, h)
-        one = ob.backward_rows(dy_shards[k].reshape(-1, h), C.f32(rows(fwd["z"])),
-                               rows(fwd["mask"]).cpu().numpy(),
-                               None if w.norm != "layernorm" else fwd["mean"][k].reshape(-1).cpu().numpy(),
-                               fwd["rstd"][k].reshape(-1).cpu().numpy(), g,
-                               None if skip is None else C.f32(rows(skip)), p=w.p, norm=w.norm)
-        sel = np.arange(n) if tokens is None else tokens[(tokens >= 0) & (tokens < n)]
-        dres = compare.bf16_bits(out["dres"][k].reshape(-1, h))
-        C.assert_bf16(dres[sel], one["dz"][sel], one["dz_magnitude"][sel], f"dresidual[{k}]")
-        for j, dg in enumerate(out["dgat"]):
-            blk = compare.bf16_bits(dg[:, offs[k]:offs[k + 1], :].reshape(-1, h))
-            C.assert_bf16(blk[sel], one["dypre_exact"][sel], one["dz_magnitude"][sel] * scale,
-                          f"dgathered[{j}] shard {k}")
-        for name in acc:
-            terms = one[name + "_terms"]
-            if terms is not None:
-                acc[name] += terms.sum(axis=0)
-                sq[name] += (terms * terms).sum(axis=0)
-    for name in ("dgamma", "dbias") + (("dbeta",) if w.norm == "layernorm" else ()):
-        bad = compare.colsum_mismatch(out[name].cpu().numpy(), acc[name], np.sqrt(sq[name]))
-        assert not bad.any(), name
+_rs_bwd_check = C.rs_bwd_check
 
 
 def _run_rs_bwd(w, fwd, inp, parts, skip, n_gather=1):
