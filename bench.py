@@ -261,7 +261,9 @@ class Step:
         sizes = w.shard_sizes()
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
         self.z = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
-        self.mask = [e((w.b, n, w.h), torch.uint8) for n in sizes]
+        # mask-free step: the forward stores no mask, the backward draws it again
+        self.mask = (None if mask == "regen" else
+                     [e((w.b, n, w.h), torch.uint8) for n in sizes])
         self.mean = [e((w.b, n), torch.float32) for n in sizes]
         self.rstd = [e((w.b, n), torch.float32) for n in sizes]
         self.gathered = [e((w.b, w.s, w.h), torch.bfloat16) for _ in range(n_gather)]
@@ -293,8 +295,8 @@ class Step:
             return
         self.sp.sp_rs_norm_fwd(i["partials"], i["residual"], i["bias"], i["gamma"], i["beta"],
                                eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
-                               cu_seqlens=self.cu, z_out=self.z, mask_out=self.mask, mean_out=self.mean,
-                               rstd_out=self.rstd, gathered=self.gathered)
+                               cu_seqlens=self.cu, z_out=self.z, mask_out=self.mask,
+                               mean_out=self.mean, rstd_out=self.rstd, gathered=self.gathered)
 
     def bwd(self):
         w = self.w
@@ -649,6 +651,8 @@ def run_ours(args):
     if args.norm is not None:
         w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
                     name=f"{w.name}-{args.norm}")
+    if args.mask == "regen" and args.bwd_entry == "g":
+        raise SystemExit("--mask regen: the backward through g reads the stored mask")
     kw = dict(n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
               bwd_entry=args.bwd_entry)
     buckets = None
@@ -672,8 +676,9 @@ def run_ours(args):
     tokens = w.tokens * args.steps * world
     value = tokens / (total_ms / 1e3)
     fused = args.pipeline == "fused"
-    fb = (fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
-          unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm)) * w.tokens
+    fb = ((fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
+           unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm))
+          - (w.h if args.mask == "regen" else 0)) * w.tokens
     if args.bwd_entry == "g":
         bb = bwd_g_bytes_per_token(w.t, w.h, args.n_gather, w.norm, fused) * w.tokens
     else:
@@ -839,7 +844,8 @@ def parse_args(argv=None):
                     help="g: the backward starts from each rank's partial gradient of the "
                          "gathered input (reduce-scatter fused, or separate if unfused)")
     ap.add_argument("--mask", choices=["stored", "regen"], default="stored",
-                    help="regen: the backward draws the dropout mask again (mask-free)")
+                    help="regen: the mask-free step (the forward stores no mask, the "
+                         "backward draws it again)")
     ap.add_argument("--pipeline", choices=["fused", "unfused"], default="fused",
                     help="unfused: reduce-scatter, shard norm and all-gather as three calls")
     ap.add_argument("--bucket", action="store_true",

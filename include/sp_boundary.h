@@ -107,7 +107,10 @@ typedef enum sp_norm {
  *                packed sequence lengths; requires b == 1 and
  *                cu_seqlens[n_seqs] == s (checked on the device)
  * z_out     [t]  (b, s_k, h) bf16  Z, saved for the backward (output)
- * mask_out  [t]  (b, s_k, h) u8    1 = kept, 0 = dropped (output)
+ * mask_out  [t]  (b, s_k, h) u8    1 = kept, 0 = dropped (output); NULL (the
+ *                array): no mask is stored, h bytes less per token written and
+ *                kept -- the backward is then sp_norm_bwd_philox, which draws
+ *                the keep decisions again from (seed, offset, p)
  * mean_out  [t]  (b, s_k)    f32   LayerNorm mean; NULL (the array) for RMS
  * rstd_out  [t]  (b, s_k)    f32   rstd (output)
  * gathered  [n_gather] (b, s, h) bf16  full-sequence copies of O (output);
@@ -297,7 +300,9 @@ sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
  * stored 1-byte mask.  Because the forward's generator is counter-based and
  * keyed on the element's global index (L7 answer to Q1: one seed on every
  * rank), the same (seed, offset, p) reproduce the forward's mask exactly; the
- * backward then reads h bytes less per token.  Arguments as for sp_norm_bwd,
+ * backward then reads h bytes less per token, and a forward called with
+ * mask_out == NULL need not write or keep the mask at all (h bytes less per
+ * token in the forward and in the saved activations).  Arguments as for sp_norm_bwd,
  * minus `mask`, plus the forward's `seed` and `offset`; the workspace size is
  * sp_norm_bwd_workspace_bytes.
  */

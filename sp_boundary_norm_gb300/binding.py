@@ -166,7 +166,8 @@ def _seq_meta(cu_seqlens, b, device):
 def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offset=0,
                    cu_seqlens=None, norm="layernorm", z_out, mask_out, mean_out, rstd_out,
                    gathered, status=None):
-    """Fused g* + bias + dropout + residual + norm + g (writes the given outputs)."""
+    """Fused g* + bias + dropout + residual + norm + g (writes the given outputs;
+    mask_out=None stores no mask: the backward is then sp_norm_bwd_philox)."""
     lib = load()
     t = len(partials)
     if not 1 <= t <= MAX_RANKS:
@@ -181,7 +182,8 @@ def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offse
     for k in range(t):
         _need(residual[k], (b, sizes[k], h), bf, dev, f"residual[{k}]")
         _need(z_out[k], (b, sizes[k], h), bf, dev, f"z_out[{k}]")
-        _need(mask_out[k], (b, sizes[k], h), torch.uint8, dev, f"mask_out[{k}]")
+        if mask_out is not None:
+            _need(mask_out[k], (b, sizes[k], h), torch.uint8, dev, f"mask_out[{k}]")
         _need(rstd_out[k], (b, sizes[k]), torch.float32, dev, f"rstd_out[{k}]")
         if ln:
             _need(mean_out[k], (b, sizes[k]), torch.float32, dev, f"mean_out[{k}]")
@@ -205,7 +207,8 @@ def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offse
 def sp_shard_norm_fwd(y_shards, residual, bias, gamma, beta, *, s, eps, p, seed, offset=0,
                       cu_seqlens=None, norm="layernorm", z_out, mask_out, mean_out, rstd_out,
                       o_shards, status=None):
-    """Unfused middle step: bias + dropout + residual + norm on reduced shards."""
+    """Unfused middle step: bias + dropout + residual + norm on reduced shards
+    (mask_out=None: no mask stored, as for sp_rs_norm_fwd)."""
     lib = load()
     t = len(y_shards)
     b, _, h = y_shards[0].shape
@@ -217,7 +220,8 @@ def sp_shard_norm_fwd(y_shards, residual, bias, gamma, beta, *, s, eps, p, seed,
         for name, x in (("y_shards", y_shards), ("residual", residual), ("z_out", z_out),
                         ("o_shards", o_shards)):
             _need(x[k], (b, sizes[k], h), bf, dev, f"{name}[{k}]")
-        _need(mask_out[k], (b, sizes[k], h), torch.uint8, dev, f"mask_out[{k}]")
+        if mask_out is not None:
+            _need(mask_out[k], (b, sizes[k], h), torch.uint8, dev, f"mask_out[{k}]")
         _need(rstd_out[k], (b, sizes[k]), torch.float32, dev, f"rstd_out[{k}]")
         if ln:
             _need(mean_out[k], (b, sizes[k]), torch.float32, dev, f"mean_out[{k}]")

@@ -582,7 +582,8 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   if ((st = check_ptrs(partials, t, "partials", true)) != SP_OK) return st;
   if ((st = check_ptrs(residual, t, "residual", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(z_out, t, "z_out", true, &map)) != SP_OK) return st;
-  if ((st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
+  const bool store_mask = mask_out != nullptr;
+  if (store_mask && (st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(rstd_out, t, "rstd_out", false, &map)) != SP_OK) return st;
   if (ln && (st = check_ptrs(mean_out, t, "mean_out", false, &map)) != SP_OK) return st;
   if ((st = check_ptrs(gathered, n_gather, "gathered", true)) != SP_OK) return st;
@@ -599,7 +600,7 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
     const size_t n = static_cast<size_t>(shard_rows(map, k));
     rg.add(residual[k], n * h * 2, false, "residual", k);
     rg.add(z_out[k], n * h * 2, true, "z_out", k);
-    rg.add(mask_out[k], n * h, true, "mask_out", k);
+    if (store_mask) rg.add(mask_out[k], n * h, true, "mask_out", k);
     rg.add(rstd_out[k], n * 4, true, "rstd_out", k);
     if (ln) rg.add(mean_out[k], n * 4, true, "mean_out", k);
   }
@@ -618,7 +619,7 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   for (int k = 0; k < t; ++k) {
     P.residual[k] = static_cast<const uint16_t*>(residual[k]);
     P.z[k] = static_cast<uint16_t*>(z_out[k]);
-    P.mask[k] = mask_out[k];
+    P.mask[k] = store_mask ? mask_out[k] : nullptr;
     P.rstd[k] = rstd_out[k];
     P.mean[k] = ln ? mean_out[k] : nullptr;
   }
@@ -644,9 +645,13 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   const LaunchShape ls = fwd_shape(rows, h, t);
   g_last_shape[0] = ls;
   const int threads = ls.threads - kFwdProducerThreads;
-  const cudaError_t e = launch(ls.cluster > 1 ? fwd_kernel_pair(threads, t, ls.stages)
-                                              : fwd_kernel(threads, t, ls.stages),
-                               ls, &P, static_cast<cudaStream_t>(stream));
+  if (!store_mask && ls.cluster > 1)
+    return fail(SP_ERR_UNSUPPORTED, "the row split over a CTA pair (a tuning option) stores "
+                "the mask: mask_out must not be NULL");
+  const void* fn = !store_mask       ? fwd_nomask_kernel(threads, t, ls.stages)
+                   : ls.cluster > 1 ? fwd_kernel_pair(threads, t, ls.stages)
+                                    : fwd_kernel(threads, t, ls.stages);
+  const cudaError_t e = launch(fn, ls, &P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_fwd launch");
   return SP_OK;
 }
@@ -673,7 +678,8 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
   if ((st = check_ptrs(y_shards, t, "y_shards", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(residual, t, "residual", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(z_out, t, "z_out", true, &map)) != SP_OK) return st;
-  if ((st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
+  const bool store_mask = mask_out != nullptr;
+  if (store_mask && (st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(rstd_out, t, "rstd_out", false, &map)) != SP_OK) return st;
   if (ln && (st = check_ptrs(mean_out, t, "mean_out", false, &map)) != SP_OK) return st;
   if ((st = check_ptrs(o_shards, t, "o_shards", true, &map)) != SP_OK) return st;
@@ -688,7 +694,7 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
     rg.add(y_shards[k], n * h * 2, false, "y_shards", k);
     rg.add(residual[k], n * h * 2, false, "residual", k);
     rg.add(z_out[k], n * h * 2, true, "z_out", k);
-    rg.add(mask_out[k], n * h, true, "mask_out", k);
+    if (store_mask) rg.add(mask_out[k], n * h, true, "mask_out", k);
     rg.add(rstd_out[k], n * 4, true, "rstd_out", k);
     if (ln) rg.add(mean_out[k], n * 4, true, "mean_out", k);
     rg.add(o_shards[k], n * h * 2, true, "o_shards", k);
@@ -704,7 +710,7 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
     P.partials[k] = static_cast<const uint16_t*>(y_shards[k]);
     P.residual[k] = static_cast<const uint16_t*>(residual[k]);
     P.z[k] = static_cast<uint16_t*>(z_out[k]);
-    P.mask[k] = mask_out[k];
+    P.mask[k] = store_mask ? mask_out[k] : nullptr;
     P.rstd[k] = rstd_out[k];
     P.mean[k] = ln ? mean_out[k] : nullptr;
     P.gathered[k] = static_cast<uint16_t*>(o_shards[k]);
@@ -726,8 +732,10 @@ sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* re
   P.status = dev_status;
   P.withhold = withhold ? 1 : 0;
   const LaunchShape ls = fwd_shard_shape(P.rows, h);
-  const cudaError_t e = launch(fwd_shard_kernel(ls.threads - kFwdProducerThreads, ls.stages), ls, &P,
-                               static_cast<cudaStream_t>(stream));
+  const int threads = ls.threads - kFwdProducerThreads;
+  const void* fn = store_mask ? fwd_shard_kernel(threads, ls.stages)
+                              : fwd_shard_nomask_kernel(threads, ls.stages);
+  const cudaError_t e = launch(fn, ls, &P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_shard_norm_fwd launch");
   return SP_OK;
 }

@@ -21,7 +21,9 @@ namespace spb {
 // the same order (CTA 0's part first), so both normalise with the same
 // statistics.  Launched with a cluster dimension of 2; CTA 0 stores mean and
 // rstd.
-template <int NTHR, int STAGES, int TT, bool SHARD, int CL = 1>
+// MASK = false: no dropout mask is stored (the mask-free pipeline, whose
+// backward draws the keep decisions again).
+template <int NTHR, int STAGES, int TT, bool SHARD, int CL = 1, bool MASK = true>
 __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     rs_norm_fwd_kernel(const FwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     const int k = cur.k;
     const int64_t local = cur.local;
     uint16_t* zrow = P.z[k] + local * h + coff + c0;
-    uint8_t* mrow = P.mask[k] + local * h + coff + c0;
+    uint8_t* mrow = MASK ? P.mask[k] + local * h + coff + c0 : nullptr;
     const uint64_t e_row = static_cast<uint64_t>(row * h + coff + c0);   // global element index
 
     // ---- pass 1: g* sum, bias, dropout, residual -> Z (stored) ----------
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
         const uint4 bv = ldg16(P.bias + coff + cc + c0);
         add8_bf16(bv, y);   // + bias
         // dropout: element e keeps iff its Philox word >= thr
-        uint2 keep = make_uint2(0x01010101u, 0x01010101u);
+        [[maybe_unused]] uint2 keep = make_uint2(0x01010101u, 0x01010101u);   // mask bytes
         if (P.thr) {
           const uint64_t q = (e_row + cc) >> 2;
           const uint4 a = philox4x32_10(make_uint4(static_cast<uint32_t>(q),
@@ -246,13 +248,13 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
           for (int e = 0; e < 8; e += 2) mul2_to(y[e], y[e + 1], P.scale, ys[e], ys[e + 1]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) y[e] = (u[e] >= P.thr) ? ys[e] : 0.f;
-          keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
+          if constexpr (MASK) keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         }
         // (with p == 0 the scale is exactly 1 and y * 1 == y)
         add8_bf16(rv, y);   // + residual -> Z in fp32
         const uint4 zb = pack8(y);                 // Z = bf16_rne(...)
         st16_stream(zrow + cc, zb);
-        st8_stream(mrow + cc, keep);
+        if constexpr (MASK) st8_stream(mrow + cc, keep);
         *reinterpret_cast<uint4*>(zbuf + ch * kStream) = zb;
         // the norm sees the stored bf16 values: sum of Z (LayerNorm) and sum
         // of Z^2 (both norms)

@@ -159,6 +159,9 @@ const void* fwd_kernel(int threads, int t, int stages);
 // The forward with each row split over a cluster of two CTAs (threads 128 or 256).
 const void* fwd_kernel_pair(int threads, int t, int stages);
 const void* fwd_shard_kernel(int threads, int stages);
+// The same two forwards storing no dropout mask (no cluster variant).
+const void* fwd_nomask_kernel(int threads, int t, int stages);
+const void* fwd_shard_nomask_kernel(int threads, int stages);
 const void* bwd_kernel(int threads, int maxc, int ring);
 const void* bwd_regen_kernel(int threads, int maxc, int ring);
 // The stored-mask backward sending dYpre to its gathered copies with bulk copies.

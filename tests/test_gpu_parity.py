@@ -814,6 +814,64 @@ def test_mask_free_backward_equals_stored_mask_backward(variant, with_skip):
     C.check_param_grads(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], got)
 
 
+@pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(b=2, s=40, t=4),
+                                     dict(p=0.0), dict(h=5120, s=24), dict(n_gather=3),
+                                     dict(seqlens=(5, 17, 3, 40, 1, 9), s=75, t=4, h=256)])
+@pytest.mark.parametrize("pipeline", ["fused", "unfused"])
+def test_forward_without_mask_then_mask_free_backward(variant, pipeline):
+    """mask_out = NULL: the forward writes Z, the statistics and O bit for bit
+    as it does with the mask, and stores no mask; the mask-free backward of
+    its outputs matches the oracle's backward of the stored-mask forward."""
+    w = wl.Workload("nm", t=2, b=1, s=64, h=512, draw_seed=72).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+    ng = max(1, w.n_gather)
+    if pipeline == "fused":
+        ref = C.run_fwd(w, inp, n_gather=ng)
+        got = C.alloc_fwd(w, ng, fill=7.0)
+        C.sp.sp_rs_norm_fwd(inp["partials"], inp["residual"], inp["bias"], inp["gamma"],
+                            inp["beta"], eps=w.eps, p=w.p, seed=w.seed, offset=w.offset,
+                            norm=w.norm, cu_seqlens=cu, z_out=got["z"], mask_out=None,
+                            mean_out=got["mean"], rstd_out=got["rstd"], gathered=got["gathered"])
+        pairs = [("z", ref["z"], got["z"]), ("gathered", ref["gathered"], got["gathered"])]
+    else:
+        y, o_ref, ref = C.run_unfused(w, inp, n_gather=0)
+        got = C.alloc_fwd(w, 0, fill=7.0)
+        o_got = [torch.full_like(x, 7.0) for x in o_ref]
+        C.sp.sp_shard_norm_fwd(y, inp["residual"], inp["bias"], inp["gamma"], inp["beta"],
+                               s=w.s, eps=w.eps, p=w.p, seed=w.seed, offset=w.offset,
+                               norm=w.norm, cu_seqlens=cu, z_out=got["z"], mask_out=None,
+                               mean_out=got["mean"], rstd_out=got["rstd"], o_shards=o_got)
+        pairs = [("z", ref["z"], got["z"]), ("o", o_ref, o_got)]
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    pairs.append(("rstd", ref["rstd"], got["rstd"]))
+    if w.norm == "layernorm":
+        pairs.append(("mean", ref["mean"], got["mean"]))
+    for name, a_list, b_list in pairs:
+        for a, b in zip(a_list, b_list):
+            assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else
+                               a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else
+                               b.view(torch.int32)), name
+    if pipeline == "fused":
+        C.fwd_compare_all(w, inp, ref)
+
+    bi = wl.backward_inputs(w, C.DEV)
+    mf = C.alloc_bwd(w, 1)
+    C.sp.sp_norm_bwd_philox(bi["dy"], got["z"], got["mean"], got["rstd"], inp["gamma"], None,
+                            s=w.s, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                            cu_seqlens=cu, dresidual=mf["dres"], dgathered=mf["dgat"],
+                            dgamma=mf["dgamma"],
+                            dbeta=mf["dbeta"] if w.norm == "layernorm" else None,
+                            dbias=mf["dbias"], workspace=mf["ws"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    # the oracle backward reads the stored-mask forward's mask
+    C.check_bwd_rows(w, ref, inp["gamma"], bi["dy"], None, mf, np.arange(w.tokens))
+    C.check_param_grads(w, ref, inp["gamma"], bi["dy"], None, mf)
+
+
 def test_mask_free_backward_70b_sampled():
     w = wl.WORKLOADS["bwd70b"]
     inp = wl.forward_inputs(w, C.DEV)

@@ -11,11 +11,12 @@ skip-path gradient.  Per case:
   - the fused forward: Z and the mask bit for bit, statistics at 1e-5, every
     gathered copy at the bf16 bar ("第 7 课：序列并行 SP" §2 and §3: the
     token-wise operators give the same result on whichever rank holds the
-    token);
+    token); and the same forward storing no mask, bit for bit the same;
   - the unfused forward (reduce-scatter, norm on the shards, all-gather) on the
     same inputs, against the oracle from its bf16 shard sums;
-  - the backward from the shards with the stored mask and the mask-free one,
-    every dResidual / dYpre element and the parameter-gradient column sums;
+  - the backward from the shards with the stored mask, and the mask-free one
+    from the forward that stored none, every dResidual / dYpre element and the
+    parameter-gradient column sums;
   - the backward entered through g (t partial gradients reduce-scattered), or,
     for the shapes whose partial stages do not fit one SM's shared memory,
     the documented refusal with nothing written.
@@ -112,6 +113,19 @@ def test_random_shape_every_entry_point_every_element(gpu, i):
     C.sp.check_device_status(C.DEV)
     C.fwd_compare_all(w, inp, fwd)
 
+    # the same forward storing no mask: the same bits everywhere else
+    nm = C.alloc_fwd(w, w.n_gather, fill=7.0)
+    C.sp.sp_rs_norm_fwd(inp["partials"], inp["residual"], inp["bias"], inp["gamma"], inp["beta"],
+                        eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
+                        cu_seqlens=cu, z_out=nm["z"], mask_out=None, mean_out=nm["mean"],
+                        rstd_out=nm["rstd"], gathered=nm["gathered"])
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    for key in ("z", "gathered", "rstd") + (("mean",) if w.norm == "layernorm" else ()):
+        for a, b in zip(fwd[key], nm[key]):
+            assert torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                               b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)), key
+
     # unfused forward: reduce-scatter, norm on the shards, all-gather
     y, o, un = C.run_unfused(w, inp, n_gather=max(1, w.n_gather))
     torch.cuda.synchronize()
@@ -128,8 +142,8 @@ def test_random_shape_every_entry_point_every_element(gpu, i):
     C.check_bwd_rows(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], out, tokens)
     C.check_param_grads(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], out)
 
-    mf = C.alloc_bwd(w, n_gather_bwd)
-    C.sp.sp_norm_bwd_philox(bi["dy"], fwd["z"], fwd["mean"], fwd["rstd"], inp["gamma"],
+    mf = C.alloc_bwd(w, n_gather_bwd)   # from the forward that stored no mask
+    C.sp.sp_norm_bwd_philox(bi["dy"], nm["z"], nm["mean"], nm["rstd"], inp["gamma"],
                             bi["dz_skip"], s=w.s, p=w.p, seed=w.seed, offset=w.offset,
                             norm=w.norm, cu_seqlens=cu, dresidual=mf["dres"],
                             dgathered=mf["dgat"], dgamma=mf["dgamma"],
