@@ -261,9 +261,11 @@ class Step:
         sizes = w.shard_sizes()
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
         self.z = [e((w.b, n, w.h), torch.bfloat16) for n in sizes]
-        # mask-free step: the forward stores no mask, the backward draws it again
+        # mask-free step: the forward stores no mask, the backward draws it
+        # again; "bits": the mask stored one bit per element
         self.mask = (None if mask == "regen" else
-                     [e((w.b, n, w.h), torch.uint8) for n in sizes])
+                     [e((w.b, n, w.h // 8 if mask == "bits" else w.h), torch.uint8)
+                      for n in sizes])
         self.mean = [e((w.b, n), torch.float32) for n in sizes]
         self.rstd = [e((w.b, n), torch.float32) for n in sizes]
         self.gathered = [e((w.b, w.s, w.h), torch.bfloat16) for _ in range(n_gather)]
@@ -293,6 +295,13 @@ class Step:
             if self.gathered:
                 self.sp.sp_allgather_seq(self.o, self.gathered, s=w.s, cu_seqlens=self.cu)
             return
+        if self.mask_mode == "bits":
+            self.sp.sp_rs_norm_fwd_bitmask(
+                i["partials"], i["residual"], i["bias"], i["gamma"], i["beta"], eps=w.eps,
+                p=w.p, seed=w.seed, offset=w.offset, norm=w.norm, cu_seqlens=self.cu,
+                z_out=self.z, mask_bits_out=self.mask, mean_out=self.mean, rstd_out=self.rstd,
+                gathered=self.gathered)
+            return
         self.sp.sp_rs_norm_fwd(i["partials"], i["residual"], i["bias"], i["gamma"], i["beta"],
                                eps=w.eps, p=w.p, seed=w.seed, offset=w.offset, norm=w.norm,
                                cu_seqlens=self.cu, z_out=self.z, mask_out=self.mask,
@@ -317,11 +326,10 @@ class Step:
                 dresidual=self.dres, dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
                 dbias=self.dbias, workspace=self.ws)
             return
-        self.sp.sp_norm_bwd(self.dy, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"],
-                            None, s=w.s, p=w.p, norm=w.norm, cu_seqlens=self.cu,
-                            dresidual=self.dres,
-                            dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
-                            dbias=self.dbias, workspace=self.ws)
+        bwd = self.sp.sp_norm_bwd_bitmask if self.mask_mode == "bits" else self.sp.sp_norm_bwd
+        bwd(self.dy, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"], None, s=w.s,
+            p=w.p, norm=w.norm, cu_seqlens=self.cu, dresidual=self.dres, dgathered=self.dgat,
+            dgamma=self.dgamma, dbeta=self.dbeta, dbias=self.dbias, workspace=self.ws)
 
 
     def inputs(self):
@@ -651,8 +659,10 @@ def run_ours(args):
     if args.norm is not None:
         w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
                     name=f"{w.name}-{args.norm}")
-    if args.mask == "regen" and args.bwd_entry == "g":
-        raise SystemExit("--mask regen: the backward through g reads the stored mask")
+    if args.mask != "stored" and args.bwd_entry == "g":
+        raise SystemExit("--mask regen / bits: the backward through g reads the byte mask")
+    if args.mask == "bits" and args.pipeline != "fused":
+        raise SystemExit("--mask bits: the fused forward only")
     kw = dict(n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
               bwd_entry=args.bwd_entry)
     buckets = None
@@ -676,14 +686,13 @@ def run_ours(args):
     tokens = w.tokens * args.steps * world
     value = tokens / (total_ms / 1e3)
     fused = args.pipeline == "fused"
+    mask_less = {"stored": 0, "regen": w.h, "bits": w.h - w.h // 8}[args.mask]
     fb = ((fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
-           unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm))
-          - (w.h if args.mask == "regen" else 0)) * w.tokens
+           unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm)) - mask_less) * w.tokens
     if args.bwd_entry == "g":
         bb = bwd_g_bytes_per_token(w.t, w.h, args.n_gather, w.norm, fused) * w.tokens
     else:
-        bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm)
-              - (w.h if args.mask == "regen" else 0)) * w.tokens
+        bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm) - mask_less) * w.tokens
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     peak, peak_kind = measured_peak()
@@ -843,9 +852,10 @@ def parse_args(argv=None):
     ap.add_argument("--bwd-entry", choices=["shard", "g"], default="shard",
                     help="g: the backward starts from each rank's partial gradient of the "
                          "gathered input (reduce-scatter fused, or separate if unfused)")
-    ap.add_argument("--mask", choices=["stored", "regen"], default="stored",
+    ap.add_argument("--mask", choices=["stored", "regen", "bits"], default="stored",
                     help="regen: the mask-free step (the forward stores no mask, the "
-                         "backward draws it again)")
+                         "backward draws it again); bits: the mask stored one bit per "
+                         "element")
     ap.add_argument("--pipeline", choices=["fused", "unfused"], default="fused",
                     help="unfused: reduce-scatter, shard norm and all-gather as three calls")
     ap.add_argument("--bucket", action="store_true",

@@ -62,6 +62,24 @@ def dropout_threshold(p):
     return int(math.floor(p * 4294967296.0))
 
 
+def pack_mask_bits(mask):
+    """The mask stored one bit per element: (..., h) 0/1 bytes -> (..., h / 8)
+    uint8, byte j holding channels [8j, 8j + 8) with channel 8j + e in bit e
+    (value 2**e).  The pages keep one byte per element (L7 "具体演示与数值推演");
+    this packed layout is one the implementation adds, with the same keep
+    decisions, so it is written here from its own definition: the byte is the
+    sum of its channels' bits, each shifted to its place.  Requires h % 8 == 0."""
+    m = np.asarray(mask)
+    h = m.shape[-1]
+    if h % 8:
+        raise ValueError("h must be a multiple of 8")
+    groups = m.reshape(m.shape[:-1] + (h // 8, 8)).astype(np.uint32)
+    packed = np.zeros(groups.shape[:-1], dtype=np.uint32)
+    for e in range(8):
+        packed += (groups[..., e] & 1) << e
+    return packed.astype(np.uint8)
+
+
 def dropout_scale(p):
     """Inverted-dropout scale 1/(1-p), computed in double, stored as float32."""
     return np.float32(1.0 / (1.0 - p))

@@ -67,6 +67,10 @@ def load():
         _u64, _u64, _vp, _i32, _i32, _PP, _PP, _PP, _PP, _PP, _vp, _vp]
     lib.sp_rs_norm_bwd.restype = _i32
     lib.sp_rs_norm_bwd.argtypes = list(lib.sp_norm_bwd.argtypes)
+    lib.sp_norm_bwd_bitmask.restype = _i32
+    lib.sp_norm_bwd_bitmask.argtypes = list(lib.sp_norm_bwd.argtypes)
+    lib.sp_rs_norm_fwd_bitmask.restype = _i32
+    lib.sp_rs_norm_fwd_bitmask.argtypes = list(lib.sp_rs_norm_fwd.argtypes)
     lib.sp_norm_bwd_philox.restype = _i32
     lib.sp_norm_bwd_philox.argtypes = [
         _PP, _PP, _PP, _PP, _vp, _PP, _i64, _i64, _i64, _i32, ctypes.c_double, _u64, _u64, _vp,
@@ -168,6 +172,26 @@ def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offse
                    gathered, status=None):
     """Fused g* + bias + dropout + residual + norm + g (writes the given outputs;
     mask_out=None stores no mask: the backward is then sp_norm_bwd_philox)."""
+    _rs_norm_fwd_call("sp_rs_norm_fwd", 1, partials, residual, bias, gamma, beta, eps, p, seed,
+                      offset, cu_seqlens, norm, z_out, mask_out, mean_out, rstd_out, gathered,
+                      status)
+
+
+def sp_rs_norm_fwd_bitmask(partials, residual, bias, gamma, beta, *, eps, p, seed, offset=0,
+                           cu_seqlens=None, norm="layernorm", z_out, mask_bits_out, mean_out,
+                           rstd_out, gathered, status=None):
+    """sp_rs_norm_fwd storing the mask one bit per element
+    (mask_bits_out[k]: (b, s_k, h / 8) uint8, bit e of byte j = channel 8j + e)."""
+    if mask_bits_out is None:
+        raise ValueError("mask_bits_out is required")
+    _rs_norm_fwd_call("sp_rs_norm_fwd_bitmask", 8, partials, residual, bias, gamma, beta, eps,
+                      p, seed, offset, cu_seqlens, norm, z_out, mask_bits_out, mean_out,
+                      rstd_out, gathered, status)
+
+
+def _rs_norm_fwd_call(entry, mask_div, partials, residual, bias, gamma, beta, eps, p, seed,
+                      offset, cu_seqlens, norm, z_out, mask_out, mean_out, rstd_out, gathered,
+                      status):
     lib = load()
     t = len(partials)
     if not 1 <= t <= MAX_RANKS:
@@ -183,7 +207,7 @@ def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offse
         _need(residual[k], (b, sizes[k], h), bf, dev, f"residual[{k}]")
         _need(z_out[k], (b, sizes[k], h), bf, dev, f"z_out[{k}]")
         if mask_out is not None:
-            _need(mask_out[k], (b, sizes[k], h), torch.uint8, dev, f"mask_out[{k}]")
+            _need(mask_out[k], (b, sizes[k], h // mask_div), torch.uint8, dev, f"mask_out[{k}]")
         _need(rstd_out[k], (b, sizes[k]), torch.float32, dev, f"rstd_out[{k}]")
         if ln:
             _need(mean_out[k], (b, sizes[k]), torch.float32, dev, f"mean_out[{k}]")
@@ -195,7 +219,7 @@ def sp_rs_norm_fwd(partials, residual, bias, gamma, beta, *, eps, p, seed, offse
         _need(beta, (h,), bf, dev, "beta")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    code = lib.sp_rs_norm_fwd(
+    code = getattr(lib, entry)(
         _ptr_array(partials), _ptr_array(residual), _ptr(bias), _ptr(gamma),
         _ptr(beta) if ln else None, b, s, h, t, float(eps), float(p), int(seed), int(offset),
         cu, n_seqs, NORMS[norm], _ptr_array(z_out), _ptr_array(mask_out),
@@ -280,6 +304,23 @@ def sp_norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlen
                 norm="layernorm", dresidual, dgathered, dgamma=None, dbeta=None, dbias=None,
                 workspace, status=None):
     """Backward of the boundary (writes the given outputs)."""
+    _norm_bwd_call("sp_norm_bwd", 1, dy, z, mask, mean, rstd, gamma, dz_skip, s, p,
+                   cu_seqlens, norm, dresidual, dgathered, dgamma, dbeta, dbias, workspace,
+                   status)
+
+
+def sp_norm_bwd_bitmask(dy, z, mask_bits, mean, rstd, gamma, dz_skip=None, *, s, p,
+                        cu_seqlens=None, norm="layernorm", dresidual, dgathered, dgamma=None,
+                        dbeta=None, dbias=None, workspace, status=None):
+    """sp_norm_bwd reading the mask stored one bit per element
+    (mask_bits[k]: (b, s_k, h / 8) uint8, bit e of byte j = channel 8j + e)."""
+    _norm_bwd_call("sp_norm_bwd_bitmask", 8, dy, z, mask_bits, mean, rstd, gamma, dz_skip, s,
+                   p, cu_seqlens, norm, dresidual, dgathered, dgamma, dbeta, dbias, workspace,
+                   status)
+
+
+def _norm_bwd_call(entry, mask_div, dy, z, mask, mean, rstd, gamma, dz_skip, s, p, cu_seqlens,
+                   norm, dresidual, dgathered, dgamma, dbeta, dbias, workspace, status):
     lib = load()
     t = len(dy)
     b, _, h = dy[0].shape
@@ -290,7 +331,7 @@ def sp_norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlen
     for k in range(t):
         _need(dy[k], (b, sizes[k], h), bf, dev, f"dy[{k}]")
         _need(z[k], (b, sizes[k], h), bf, dev, f"z[{k}]")
-        _need(mask[k], (b, sizes[k], h), torch.uint8, dev, f"mask[{k}]")
+        _need(mask[k], (b, sizes[k], h // mask_div), torch.uint8, dev, f"mask[{k}]")
         _need(rstd[k], (b, sizes[k]), torch.float32, dev, f"rstd[{k}]")
         if ln:
             _need(mean[k], (b, sizes[k]), torch.float32, dev, f"mean[{k}]")
@@ -307,7 +348,7 @@ def sp_norm_bwd(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, cu_seqlen
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    code = lib.sp_norm_bwd(
+    code = getattr(lib, entry)(
         _ptr_array(dy), _ptr_array(z), _ptr_array(mask), _ptr_array(mean) if ln else None,
         _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), cu, n_seqs,
         NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),

@@ -436,11 +436,11 @@ LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip)
 
 // bulk: dYpre sent to the gathered copies by bulk copies from two shared
 // copies of the row (stored mask only), for calls with several copies.
-LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool regen, bool bulk) {
+LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool regen, bool bulk,
+                               bool bits) {
   int threads, maxc;
   bwd_threads(h, regen, &threads, &maxc);
-  const size_t item =
-      static_cast<size_t>(has_skip ? 3 : 2) * threads * 16 + (regen ? 0 : threads * 8);
+  const size_t item = static_cast<size_t>(bwd_item_bytes(threads, has_skip, regen, bits));
   const size_t ring_row = item * maxc;
   const size_t stage_row = static_cast<size_t>((h * 2 + 15) / 16) * 16;
   const size_t fixed = 2 * 32 * sizeof(float2) + (bulk ? 2 * stage_row : 0);
@@ -450,9 +450,10 @@ LaunchShape bwd_shape_uncached(int64_t rows, int64_t h, bool has_skip, bool rege
   // 0.191 against 0.194 ms), else two
   LaunchShape ls = pick_shape(1, threads, maxc, rows, ring_row, fixed, kBwdRing,
                               3, /*ring=*/cap == 1 ? 3 : 2, /*blocks per SM=*/cap, [&](int st) {
-                                return regen ? bwd_regen_kernel(threads, maxc, st)
-                                             : bulk ? bwd_bulk_kernel(threads, maxc, st)
-                                                    : bwd_kernel(threads, maxc, st);
+                                return regen  ? bwd_regen_kernel(threads, maxc, st)
+                                       : bits ? bwd_bits_kernel(threads, maxc, st)
+                                       : bulk ? bwd_bulk_kernel(threads, maxc, st)
+                                              : bwd_kernel(threads, maxc, st);
                               });
   if (tacc && ls.fits) {
     // The blocks of an SM share its 512 tensor-memory columns: pad the shared
@@ -481,9 +482,10 @@ LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
 }
 
 LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false,
-                      bool bulk = false) {
-  return cached_shape(3, rows, h, 0, (has_skip ? 1 : 0) | (regen ? 2 : 0) | (bulk ? 4 : 0),
-                      [&] { return bwd_shape_uncached(rows, h, has_skip, regen, bulk); });
+                      bool bulk = false, bool bits = false) {
+  return cached_shape(3, rows, h, 0,
+                      (has_skip ? 1 : 0) | (regen ? 2 : 0) | (bulk ? 4 : 0) | (bits ? 8 : 0),
+                      [&] { return bwd_shape_uncached(rows, h, has_skip, regen, bulk, bits); });
 }
 
 cudaError_t launch(const void* fn, const LaunchShape& ls, void* params, cudaStream_t st) {
@@ -558,14 +560,17 @@ using namespace spb;
 
 extern "C" {
 
-sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* residual,
-                           const void* bias, const void* gamma, const void* beta, int64_t b,
-                           int64_t s, int64_t h, int32_t t, float eps, double p, uint64_t seed,
-                           uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
-                           sp_norm_t norm, void* const* z_out, uint8_t* const* mask_out,
-                           float* const* mean_out, float* const* rstd_out,
-                           void* const* gathered, int32_t n_gather, int32_t* dev_status,
-                           void* stream) {
+// The fused forward with the mask stored as `maskf` (kMaskBytes, kMaskBits, or
+// kMaskNone when mask_out is NULL).
+static sp_status_t rs_norm_fwd_impl(const void* const* partials, const void* const* residual,
+                                    const void* bias, const void* gamma, const void* beta,
+                                    int64_t b, int64_t s, int64_t h, int32_t t, float eps,
+                                    double p, uint64_t seed, uint64_t offset,
+                                    const int32_t* cu_seqlens, int32_t n_seqs, sp_norm_t norm,
+                                    void* const* z_out, uint8_t* const* mask_out, int maskf,
+                                    float* const* mean_out, float* const* rstd_out,
+                                    void* const* gathered, int32_t n_gather,
+                                    int32_t* dev_status, void* stream) {
   sp_status_t st;
   const bool withhold = take_injected_timeout();
   if (take_injected(&st)) return st;
@@ -582,7 +587,7 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   if ((st = check_ptrs(partials, t, "partials", true)) != SP_OK) return st;
   if ((st = check_ptrs(residual, t, "residual", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(z_out, t, "z_out", true, &map)) != SP_OK) return st;
-  const bool store_mask = mask_out != nullptr;
+  const bool store_mask = maskf != kMaskNone;
   if (store_mask && (st = check_ptrs(mask_out, t, "mask_out", true, &map)) != SP_OK) return st;
   if ((st = check_ptrs(rstd_out, t, "rstd_out", false, &map)) != SP_OK) return st;
   if (ln && (st = check_ptrs(mean_out, t, "mean_out", false, &map)) != SP_OK) return st;
@@ -600,7 +605,8 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
     const size_t n = static_cast<size_t>(shard_rows(map, k));
     rg.add(residual[k], n * h * 2, false, "residual", k);
     rg.add(z_out[k], n * h * 2, true, "z_out", k);
-    if (store_mask) rg.add(mask_out[k], n * h, true, "mask_out", k);
+    if (store_mask)
+      rg.add(mask_out[k], maskf == kMaskBits ? n * h / 8 : n * h, true, "mask_out", k);
     rg.add(rstd_out[k], n * 4, true, "rstd_out", k);
     if (ln) rg.add(mean_out[k], n * 4, true, "mean_out", k);
   }
@@ -645,15 +651,49 @@ sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* resid
   const LaunchShape ls = fwd_shape(rows, h, t);
   g_last_shape[0] = ls;
   const int threads = ls.threads - kFwdProducerThreads;
-  if (!store_mask && ls.cluster > 1)
+  if (maskf != kMaskBytes && ls.cluster > 1)
     return fail(SP_ERR_UNSUPPORTED, "the row split over a CTA pair (a tuning option) stores "
-                "the mask: mask_out must not be NULL");
-  const void* fn = !store_mask       ? fwd_nomask_kernel(threads, t, ls.stages)
-                   : ls.cluster > 1 ? fwd_kernel_pair(threads, t, ls.stages)
-                                    : fwd_kernel(threads, t, ls.stages);
+                "the mask one byte per element only");
+  const void* fn = maskf == kMaskNone   ? fwd_nomask_kernel(threads, t, ls.stages)
+                   : maskf == kMaskBits ? fwd_bits_kernel(threads, t, ls.stages)
+                   : ls.cluster > 1     ? fwd_kernel_pair(threads, t, ls.stages)
+                                        : fwd_kernel(threads, t, ls.stages);
   const cudaError_t e = launch(fn, ls, &P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_fwd launch");
   return SP_OK;
+}
+
+sp_status_t sp_rs_norm_fwd(const void* const* partials, const void* const* residual,
+                           const void* bias, const void* gamma, const void* beta, int64_t b,
+                           int64_t s, int64_t h, int32_t t, float eps, double p, uint64_t seed,
+                           uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
+                           sp_norm_t norm, void* const* z_out, uint8_t* const* mask_out,
+                           float* const* mean_out, float* const* rstd_out,
+                           void* const* gathered, int32_t n_gather, int32_t* dev_status,
+                           void* stream) {
+  return rs_norm_fwd_impl(partials, residual, bias, gamma, beta, b, s, h, t, eps, p, seed,
+                          offset, cu_seqlens, n_seqs, norm, z_out, mask_out,
+                          mask_out != nullptr ? kMaskBytes : kMaskNone, mean_out, rstd_out,
+                          gathered, n_gather, dev_status, stream);
+}
+
+sp_status_t sp_rs_norm_fwd_bitmask(const void* const* partials, const void* const* residual,
+                                   const void* bias, const void* gamma, const void* beta,
+                                   int64_t b, int64_t s, int64_t h, int32_t t, float eps,
+                                   double p, uint64_t seed, uint64_t offset,
+                                   const int32_t* cu_seqlens, int32_t n_seqs, sp_norm_t norm,
+                                   void* const* z_out, uint8_t* const* mask_bits_out,
+                                   float* const* mean_out, float* const* rstd_out,
+                                   void* const* gathered, int32_t n_gather,
+                                   int32_t* dev_status, void* stream) {
+  if (mask_bits_out == nullptr)
+    return fail(SP_ERR_INVALID_ARG, "mask_bits_out array is NULL");
+  if (h % 32 != 0)
+    return fail(SP_ERR_UNSUPPORTED, "bit-packed mask: h = %lld must be a multiple of 32",
+                (long long)h);
+  return rs_norm_fwd_impl(partials, residual, bias, gamma, beta, b, s, h, t, eps, p, seed,
+                          offset, cu_seqlens, n_seqs, norm, z_out, mask_bits_out, kMaskBits,
+                          mean_out, rstd_out, gathered, n_gather, dev_status, stream);
 }
 
 sp_status_t sp_shard_norm_fwd(const void* const* y_shards, const void* const* residual,
@@ -813,8 +853,9 @@ size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, s
   // regenerated mask, or dYpre sent by bulk copies): one workspace size serves
   // every backward entry point
   int grid = 0;
-  for (int v = 0; v < 6; ++v) {   // skip gradient or not; stored, regenerated or bulk
-    const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v >> 1) == 1, (v >> 1) == 2);
+  for (int v = 0; v < 8; ++v) {   // skip gradient or not; byte mask, drawn again, bulk, bits
+    const LaunchShape ls = bwd_shape(b * s, h, (v & 1) != 0, (v >> 1) == 1, (v >> 1) == 2,
+                                     (v >> 1) == 3);
     if (ls.grid > grid) grid = ls.grid;
   }
   if (h <= 8192) {
@@ -830,7 +871,8 @@ static sp_status_t norm_bwd_common(
     const void* const* dy, const void* const* z, const uint8_t* const* mask,
     const float* const* mean, const float* const* rstd, const void* gamma,
     const void* const* dz_skip, int64_t b, int64_t s, int64_t h, int32_t t, double p,
-    bool regen, uint64_t seed, uint64_t offset, const int32_t* cu_seqlens, int32_t n_seqs,
+    bool regen, bool bits, uint64_t seed, uint64_t offset, const int32_t* cu_seqlens,
+    int32_t n_seqs,
     sp_norm_t norm, void* const* dresidual, void* const* dgathered, int32_t n_gather,
     float* dgamma, float* dbeta, float* dbias, void* workspace, size_t workspace_bytes,
     int32_t* dev_status, void* stream) {
@@ -871,12 +913,13 @@ static sp_status_t norm_bwd_common(
     return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
 
   const bool has_skip = dz_skip != nullptr;
-  // several gathered copies: the bulk-copy variant, if its shape fits
-  bool bulk = !regen && n_gather > 1;
-  LaunchShape ls = bwd_shape(rows, h, has_skip, regen, bulk);
+  // several gathered copies: the bulk-copy variant, if its shape fits (byte
+  // mask only)
+  bool bulk = !regen && !bits && n_gather > 1;
+  LaunchShape ls = bwd_shape(rows, h, has_skip, regen, bulk, bits);
   if (bulk && !ls.fits) {
     bulk = false;
-    ls = bwd_shape(rows, h, has_skip, regen, false);
+    ls = bwd_shape(rows, h, has_skip, regen, false, bits);
   }
   g_last_shape[1] = ls;
   const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
@@ -891,7 +934,7 @@ static sp_status_t norm_bwd_common(
     const size_t n = static_cast<size_t>(shard_rows(map, k));
     rg.add(dy[k], n * h * 2, false, "dy", k);
     rg.add(z[k], n * h * 2, false, "z", k);
-    if (!regen) rg.add(mask[k], n * h, false, "mask", k);
+    if (!regen) rg.add(mask[k], bits ? n * h / 8 : n * h, false, "mask", k);
     rg.add(rstd[k], n * 4, false, "rstd", k);
     if (ln) rg.add(mean[k], n * 4, false, "mean", k);
     if (has_skip) rg.add(dz_skip[k], n * h * 2, false, "dz_skip", k);
@@ -935,6 +978,7 @@ static sp_status_t norm_bwd_common(
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const void* fn = regen ? bwd_regen_kernel(ls.threads, ls.maxc, ls.stages)
+                   : bits  ? bwd_bits_kernel(ls.threads, ls.maxc, ls.stages)
                    : bulk  ? bwd_bulk_kernel(ls.threads, ls.maxc, ls.stages)
                            : bwd_kernel(ls.threads, ls.maxc, ls.stages);
   cudaError_t e = launch(fn, ls, &P, cs);
@@ -1075,9 +1119,28 @@ sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8
                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
   sp_status_t st;
   if (take_injected(&st)) return st;
-  return norm_bwd_common(dy, z, mask, mean, rstd, gamma, dz_skip, b, s, h, t, p, false, 0, 0,
-                         cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma, dbeta,
-                         dbias, workspace, workspace_bytes, dev_status, stream);
+  return norm_bwd_common(dy, z, mask, mean, rstd, gamma, dz_skip, b, s, h, t, p, false, false,
+                         0, 0, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma,
+                         dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
+}
+
+sp_status_t sp_norm_bwd_bitmask(const void* const* dy, const void* const* z,
+                                const uint8_t* const* mask_bits, const float* const* mean,
+                                const float* const* rstd, const void* gamma,
+                                const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                                int32_t t, double p, const int32_t* cu_seqlens, int32_t n_seqs,
+                                sp_norm_t norm, void* const* dresidual, void* const* dgathered,
+                                int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                void* stream) {
+  sp_status_t st;
+  if (take_injected(&st)) return st;
+  if (h % 32 != 0)
+    return fail(SP_ERR_UNSUPPORTED, "bit-packed mask: h = %lld must be a multiple of 32",
+                (long long)h);
+  return norm_bwd_common(dy, z, mask_bits, mean, rstd, gamma, dz_skip, b, s, h, t, p, false,
+                         true, 0, 0, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather,
+                         dgamma, dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
 }
 
 sp_status_t sp_norm_bwd_philox(const void* const* dy, const void* const* z,
@@ -1091,9 +1154,9 @@ sp_status_t sp_norm_bwd_philox(const void* const* dy, const void* const* z,
                                void* stream) {
   sp_status_t st;
   if (take_injected(&st)) return st;
-  return norm_bwd_common(dy, z, nullptr, mean, rstd, gamma, dz_skip, b, s, h, t, p, true, seed,
-                         offset, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma,
-                         dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
+  return norm_bwd_common(dy, z, nullptr, mean, rstd, gamma, dz_skip, b, s, h, t, p, true, false,
+                         seed, offset, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather,
+                         dgamma, dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
 }
 
 const char* sp_last_error(void) { return g_err; }

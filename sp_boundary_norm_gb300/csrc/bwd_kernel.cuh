@@ -21,7 +21,14 @@ namespace spb {
 // instead of n_gather global stores per 8 elements and no barrier is added.
 // A row buffer is rewritten two rows later, after thread 0 has seen its
 // copies finish reading it (before that row's barrier).
-template <int NTHR, int MAXC, int RING, bool REGEN, bool BULK = false>
+// BITS = true: the mask is stored one bit per element (byte j of a row holds
+// channels [8j, 8j + 8), bit e channel 8j + e; h % 32 == 0); a thread needs
+// one byte per chunk.  The bytes are staged with the row: lanes 0-7 of each
+// warp copy the warp's 32 bytes of each chunk in 4-byte pieces, and every
+// lane reads its byte after the row's block barrier (which follows the
+// copying lanes' waits); a warp passes a __syncwarp before it refills a ring
+// slot, so no lane still reads the bytes being replaced.
+template <int NTHR, int MAXC, int RING, bool REGEN, bool BULK = false, bool BITS = false>
 __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
                                             ? 512 / bwd_tmem_cols(NTHR, MAXC)
                                             : (NTHR <= 256 ? 512 / NTHR : 1))
@@ -55,9 +62,9 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
   // one staged chunk ("item") of all threads: [dY | Z | mask | skip (optional)]
   // (no mask slots in the mask-free variant)
   constexpr int v16 = NTHR * 16;
-  constexpr int off_mask = 2 * v16;
-  constexpr int off_skip = off_mask + (REGEN ? 0 : NTHR * 8);
-  const int item_bytes = off_skip + (has_skip ? v16 : 0);
+  constexpr int off_mask = bwd_item_mask_offset(NTHR);
+  constexpr int off_skip = bwd_item_skip_offset(NTHR, REGEN, BITS);
+  const int item_bytes = bwd_item_bytes(NTHR, has_skip, REGEN, BITS);
   const int row_bytes = MAXC * item_bytes;
   float2* red = reinterpret_cast<float2*>(smem + RING * row_bytes);   // [2][32]
   // BULK: two shared copies of a row's dYpre, h bf16 each (16-byte aligned)
@@ -99,7 +106,7 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
       const int64_t lo0 = pw.local * h + c0;
       const uint16_t* dyp = P.dy[k] + lo0;
       const uint16_t* zp = P.z[k] + lo0;
-      const uint8_t* mp = REGEN ? nullptr : P.mask[k] + lo0;
+      const uint8_t* mp = REGEN || BITS ? nullptr : P.mask[k] + lo0;
       uint8_t* it0 = smem + pf_slot * row_bytes + tid * 16;
 #pragma unroll
       for (int ch = 0; ch < MAXC; ++ch) {
@@ -107,8 +114,16 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
           uint8_t* it = it0 + ch * item_bytes;
           cp_async16(it, dyp + ch * kChunk);
           cp_async16(it + v16, zp + ch * kChunk);
-          if (!REGEN) cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // 8 B apart
+          if (!REGEN && !BITS) cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // 8 B apart
           if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
+        }
+        if (BITS && (tid & 31) < 8) {
+          // bytes [4 l, 4 l + 4) of this warp's 32 (lane l); with h % 32 == 0
+          // a 4-byte piece is wholly inside the row or wholly past its end
+          const int byte0 = ch * NTHR + (tid & ~31) + 4 * (tid & 31);
+          if (byte0 < h / 8)
+            cp_async4(it0 - tid * 16 + ch * item_bytes + off_mask + (byte0 - ch * NTHR),
+                      P.mask[k] + (pw.local * h) / 8 + byte0);
         }
       }
       rec.row = pw.row;
@@ -139,6 +154,7 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
   const float inv_h = 1.f / static_cast<float>(h);
   for (int64_t ri = 0; ri < nrows; ++ri) {
     // row ri + RING - 1 refills the slot row ri - 1 used
+    if constexpr (BITS) __syncwarp();   // the lanes have read the bytes it replaces
     RowRec cur;
     if (RING > 1) {
       cur = q[0];
@@ -271,6 +287,10 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
           const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) kept[e] = u[e] >= P.thr;
+        } else if (BITS) {
+          const uint32_t mbyte = it0[ch * item_bytes + off_mask - tid * 15];   // own byte
+#pragma unroll
+          for (int e = 0; e < 8; ++e) kept[e] = ((mbyte >> e) & 1u) != 0u;
         } else {
           // stored mask bytes are 0 or 1: bit 0 of byte e decides
           const uint2 mk = lds8(it + off_mask - tid * 8);

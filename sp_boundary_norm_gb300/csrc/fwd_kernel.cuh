@@ -21,9 +21,11 @@ namespace spb {
 // the same order (CTA 0's part first), so both normalise with the same
 // statistics.  Launched with a cluster dimension of 2; CTA 0 stores mean and
 // rstd.
-// MASK = false: no dropout mask is stored (the mask-free pipeline, whose
-// backward draws the keep decisions again).
-template <int NTHR, int STAGES, int TT, bool SHARD, int CL = 1, bool MASK = true>
+// MASKF: how the dropout mask is stored -- kMaskBytes (one byte per element,
+// 1 = kept), kMaskNone (not at all: the mask-free pipeline, whose backward
+// draws the keep decisions again) or kMaskBits (one bit per element: byte j
+// of a row holds channels [8j, 8j + 8), bit e channel 8j + e).
+template <int NTHR, int STAGES, int TT, bool SHARD, int CL = 1, int MASKF = kMaskBytes>
 __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     rs_norm_fwd_kernel(const FwdParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -194,7 +196,9 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
     const int k = cur.k;
     const int64_t local = cur.local;
     uint16_t* zrow = P.z[k] + local * h + coff + c0;
-    uint8_t* mrow = MASK ? P.mask[k] + local * h + coff + c0 : nullptr;
+    uint8_t* mrow = MASKF == kMaskBytes ? P.mask[k] + local * h + coff + c0
+                    : MASKF == kMaskBits ? P.mask[k] + (local * h + coff + c0) / 8
+                                         : nullptr;
     const uint64_t e_row = static_cast<uint64_t>(row * h + coff + c0);   // global element index
 
     // ---- pass 1: g* sum, bias, dropout, residual -> Z (stored) ----------
@@ -248,13 +252,15 @@ __global__ void __launch_bounds__(NTHR + kFwdProducerThreads, 512 / NTHR)
           for (int e = 0; e < 8; e += 2) mul2_to(y[e], y[e + 1], P.scale, ys[e], ys[e + 1]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) y[e] = (u[e] >= P.thr) ? ys[e] : 0.f;
-          if constexpr (MASK) keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
+          if constexpr (MASKF != kMaskNone)
+            keep = make_uint2(keep_bytes4(a, P.thr), keep_bytes4(b, P.thr));
         }
         // (with p == 0 the scale is exactly 1 and y * 1 == y)
         add8_bf16(rv, y);   // + residual -> Z in fp32
         const uint4 zb = pack8(y);                 // Z = bf16_rne(...)
         st16_stream(zrow + cc, zb);
-        if constexpr (MASK) st8_stream(mrow + cc, keep);
+        if constexpr (MASKF == kMaskBytes) st8_stream(mrow + cc, keep);
+        if constexpr (MASKF == kMaskBits) st1_stream(mrow + cc / 8, keep_bits8(keep));
         *reinterpret_cast<uint4*>(zbuf + ch * kStream) = zb;
         // the norm sees the stored bf16 values: sum of Z (LayerNorm) and sum
         // of Z^2 (both norms)

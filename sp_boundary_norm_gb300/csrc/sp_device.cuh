@@ -195,6 +195,17 @@ __device__ __forceinline__ uint32_t keep_bytes4(uint4 u, uint32_t thr) {
   return __byte_perm(__byte_perm(k0, k1, 0x3340), __byte_perm(k2, k3, 0x3340), 0x5410);
 }
 
+// The 8 keep flags of two keep_bytes4 words as one byte, element e in bit e.
+// For w = b0 + b1 2^8 + b2 2^16 + b3 2^24 (each b 0 or 1), w * (2^21 + 2^14 +
+// 2^7 + 1) holds b_i at bit 21 + i: the other partial products land at bits
+// 0-16 (their sum stays below 2^17, so nothing carries into bit 21) or at
+// bit 29 and above.
+__device__ __forceinline__ uint32_t keep_bits8(uint2 kb) {
+  constexpr uint32_t kGather = (1u << 21) | (1u << 14) | (1u << 7) | 1u;
+  const uint32_t lo = (kb.x * kGather) >> 21 & 0xFu, hi = (kb.y * kGather) >> 21 & 0xFu;
+  return lo | (hi << 4);
+}
+
 
 
 
@@ -211,6 +222,13 @@ __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_gmem)
 }
 
 // 8-byte global -> shared asynchronous copy.
+// 4-byte global -> shared asynchronous copy (both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_addr(dst_smem)),
+               "l"(src_gmem)
+               : "memory");
+}
+
 __device__ __forceinline__ void cp_async8(void* dst_smem, const void* src_gmem) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(dst_smem)),
                "l"(src_gmem)
@@ -254,6 +272,11 @@ __device__ __forceinline__ void st16_stream(void* p, uint4 v) {
 
 __device__ __forceinline__ void st8_stream(void* p, uint2 v) {
   __stcs(reinterpret_cast<uint2*>(p), v);
+}
+
+// Streaming one-byte store (the low byte of v).
+__device__ __forceinline__ void st1_stream(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ------------------------------------------ programmatic dependent launch --

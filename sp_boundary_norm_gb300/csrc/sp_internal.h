@@ -33,6 +33,19 @@ __host__ __device__ constexpr int bwd_tmem_cols(int nthr, int maxc) {
   return c;
 }
 
+// The backward's staged chunk of one row ("item"), shared by the kernel's
+// shared-memory layout and the host's launch-shape choice: dY and Z (16 bytes
+// per thread each), then the mask (8 bytes per thread as bytes, one byte per
+// thread as bits, none when drawn again), then the optional skip gradient
+// (16 bytes per thread).  Offsets of the mask and the skip gradient inside it:
+__host__ __device__ constexpr int bwd_item_mask_offset(int nthr) { return 2 * nthr * 16; }
+__host__ __device__ constexpr int bwd_item_skip_offset(int nthr, bool regen, bool bits) {
+  return bwd_item_mask_offset(nthr) + (regen ? 0 : bits ? nthr : nthr * 8);
+}
+__host__ __device__ constexpr int bwd_item_bytes(int nthr, bool has_skip, bool regen, bool bits) {
+  return bwd_item_skip_offset(nthr, regen, bits) + (has_skip ? nthr * 16 : 0);
+}
+
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
@@ -54,6 +67,11 @@ struct ShardMap {
   int64_t b, s, h;
   int32_t t;
 };
+
+// How a forward stores the dropout mask.
+constexpr int kMaskNone = 0;    // not at all
+constexpr int kMaskBytes = 1;   // one byte per element, 1 = kept
+constexpr int kMaskBits = 2;    // one bit per element, 8 channels per byte
 
 // The forward's blocks add one copy-producer warp to their compute threads.
 constexpr int kFwdProducerThreads = 32;
@@ -162,10 +180,14 @@ const void* fwd_shard_kernel(int threads, int stages);
 // The same two forwards storing no dropout mask (no cluster variant).
 const void* fwd_nomask_kernel(int threads, int t, int stages);
 const void* fwd_shard_nomask_kernel(int threads, int stages);
+// The fused forward storing the mask one bit per element (no cluster variant).
+const void* fwd_bits_kernel(int threads, int t, int stages);
 const void* bwd_kernel(int threads, int maxc, int ring);
 const void* bwd_regen_kernel(int threads, int maxc, int ring);
 // The stored-mask backward sending dYpre to its gathered copies with bulk copies.
 const void* bwd_bulk_kernel(int threads, int maxc, int ring);
+// The backward reading the mask stored one bit per element.
+const void* bwd_bits_kernel(int threads, int maxc, int ring);
 // Backward entered through g (reduce-scatter of t partial gradients fused):
 // (threads, chunks per row, ranks t, chunk stages).
 const void* rs_bwd_kernel(int threads, int maxc, int t, int stages);

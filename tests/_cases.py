@@ -160,6 +160,53 @@ def rs_bwd_check(w, fwd, inp, parts, skip, out, tokens=None):
         assert not bad.any(), name
 
 
+def bits_equal(a, b):
+    """Bit-for-bit equality of two tensors (bf16 and float32 compared as integers)."""
+    view = {torch.bfloat16: torch.int16, torch.float32: torch.int32}
+    if a.dtype in view:
+        a, b = a.view(view[a.dtype]), b.view(view[b.dtype])
+    return torch.equal(a, b)
+
+
+def run_bitmask_pair(w, inp, dy, dz_skip, n_gather_fwd, n_gather_bwd, cu_seqlens=None):
+    """The forward storing the mask one bit per element and the backward
+    reading it.  Returns (fwd outputs with "mask_bits", bwd outputs)."""
+    sizes = w.shard_sizes()
+    fwd = alloc_fwd(w, n_gather_fwd, fill=7.0)
+    fwd["mask_bits"] = [torch.full((w.b, n, w.h // 8), 0xAB, dtype=torch.uint8, device=DEV)
+                        for n in sizes]
+    sp.sp_rs_norm_fwd_bitmask(inp["partials"], inp["residual"], inp["bias"], inp["gamma"],
+                              inp["beta"], eps=w.eps, p=w.p, seed=w.seed, offset=w.offset,
+                              norm=w.norm, cu_seqlens=cu_seqlens, z_out=fwd["z"],
+                              mask_bits_out=fwd["mask_bits"], mean_out=fwd["mean"],
+                              rstd_out=fwd["rstd"], gathered=fwd["gathered"])
+    bwd = alloc_bwd(w, n_gather_bwd)
+    sp.sp_norm_bwd_bitmask(dy, fwd["z"], fwd["mask_bits"], fwd["mean"], fwd["rstd"],
+                           inp["gamma"], dz_skip, s=w.s, p=w.p, norm=w.norm,
+                           cu_seqlens=cu_seqlens, dresidual=bwd["dres"], dgathered=bwd["dgat"],
+                           dgamma=bwd["dgamma"],
+                           dbeta=bwd["dbeta"] if w.norm == "layernorm" else None,
+                           dbias=bwd["dbias"], workspace=bwd["ws"])
+    return fwd, bwd
+
+
+def assert_bitmask_pair_matches(w, fwd_bytes, bwd_bytes, fwd_bits, bwd_bits):
+    """The bit-mask pair against the byte-mask pair: the bits are the byte
+    mask packed by the oracle's definition, every other output bit for bit."""
+    for k in range(w.t):
+        want = ob.pack_mask_bits(fwd_bytes["mask"][k].cpu().numpy())
+        assert np.array_equal(fwd_bits["mask_bits"][k].cpu().numpy(), want), f"mask bits {k}"
+    keys = ["z", "rstd", "gathered"] + (["mean"] if w.norm == "layernorm" else [])
+    for key in keys:
+        for a, b in zip(fwd_bytes[key], fwd_bits[key]):
+            assert bits_equal(a, b), key
+    for key in ("dres", "dgat"):
+        for a, b in zip(bwd_bytes[key], bwd_bits[key]):
+            assert bits_equal(a, b), key
+    for key in ("dgamma", "dbias") + (("dbeta",) if w.norm == "layernorm" else ()):
+        assert bits_equal(bwd_bytes[key], bwd_bits[key]), key
+
+
 def token_shard(w, g):
     """(shard k, local row) of global token g for b == 1 or dense b > 1."""
     bi, si = divmod(int(g), w.s)

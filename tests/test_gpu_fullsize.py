@@ -147,3 +147,20 @@ def test_unfused_pipeline_full_size_every_element(name):
     t0 = time.perf_counter()
     tot = C.full_unfused_fwd_check(w, inp, y, o, out)
     print(f"\nfull-size unfused forward {name}: {tot} ({time.perf_counter() - t0:.1f} s)")
+
+
+@pytest.mark.parametrize("name", ["70b", "ragged"])
+def test_bit_mask_pair_full_size_equals_byte_mask_pair(name):
+    """At full size the bit-mask forward and backward give the byte mask packed
+    and every other output bit for bit as the byte-mask pair, which the
+    tests above check against the oracle on every element."""
+    w = wl.WORKLOADS[name]
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+    inp = wl.forward_inputs(w, C.DEV)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    fwd_b = C.run_fwd(w, inp, n_gather=1)
+    bwd_b = C.run_bwd(w, fwd_b, inp["gamma"], dy, None, n_gather=1)
+    fwd_k, bwd_k = C.run_bitmask_pair(w, inp, dy, None, 1, 1, cu_seqlens=cu)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.assert_bitmask_pair_matches(w, fwd_b, bwd_b, fwd_k, bwd_k)

@@ -872,6 +872,57 @@ def test_forward_without_mask_then_mask_free_backward(variant, pipeline):
     C.check_param_grads(w, ref, inp["gamma"], bi["dy"], None, mf)
 
 
+@pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(b=2, s=40, t=4),
+                                     dict(p=0.0), dict(p=0.9), dict(h=5120, s=24),
+                                     dict(h=96, s=16), dict(h=544, s=32), dict(h=16384, s=8),
+                                     dict(n_gather=3),
+                                     dict(seqlens=(5, 17, 3, 40, 1, 9), s=75, t=4, h=256)])
+@pytest.mark.parametrize("with_skip", [False, True])
+def test_bit_mask_forward_and_backward(variant, with_skip):
+    """The mask stored one bit per element: the forward's bits are the
+    oracle-checked byte mask packed by the oracle's definition, its other
+    outputs and the backward reading the bits are bit for bit those of the
+    byte-mask pair (same launch shapes, same summation order)."""
+    w = wl.Workload("bm", t=2, b=1, s=64, h=512, draw_seed=74).with_(**variant)
+    inp = wl.forward_inputs(w, C.DEV)
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+    bi = wl.backward_inputs(w, C.DEV, with_skip=with_skip)
+    ng = max(1, w.n_gather)
+    fwd_b = C.run_fwd(w, inp, n_gather=ng)
+    bwd_b = C.run_bwd(w, fwd_b, inp["gamma"], bi["dy"], bi["dz_skip"], n_gather=ng)
+    fwd_k, bwd_k = C.run_bitmask_pair(w, inp, bi["dy"], bi["dz_skip"], ng, ng, cu_seqlens=cu)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.fwd_compare_all(w, inp, fwd_b)
+    C.assert_bitmask_pair_matches(w, fwd_b, bwd_b, fwd_k, bwd_k)
+
+
+@pytest.mark.parametrize("h", [8, 520, 1000])
+def test_bit_mask_refuses_widths_not_a_multiple_of_32(h):
+    """The bit-packed mask needs whole 4-byte words of bits per row: other
+    widths are refused by both entry points before anything is enqueued, and
+    the outputs stay untouched."""
+    w = wl.Workload("bx", t=2, b=1, s=16, h=h, draw_seed=75)
+    inp = wl.forward_inputs(w, C.DEV)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    with pytest.raises(C.sp.SpError) as e:
+        C.run_bitmask_pair(w, inp, dy, None, 1, 1)
+    assert e.value.name == "SP_ERR_UNSUPPORTED"
+    fwd = C.run_fwd(w, inp, n_gather=1)
+    out = C.alloc_bwd(w, 1)
+    for x in out["dres"]:
+        x.fill_(3.0)
+    bits = [torch.zeros((w.b, n, h // 8), dtype=torch.uint8, device=C.DEV)
+            for n in w.shard_sizes()]
+    with pytest.raises(C.sp.SpError) as e:
+        C.sp.sp_norm_bwd_bitmask(dy, fwd["z"], bits, fwd["mean"], fwd["rstd"], inp["gamma"],
+                                 None, s=w.s, p=w.p, norm=w.norm, dresidual=out["dres"],
+                                 dgathered=out["dgat"], workspace=out["ws"])
+    assert e.value.name == "SP_ERR_UNSUPPORTED"
+    torch.cuda.synchronize()
+    assert all(bool((x == 3.0).all()) for x in out["dres"])
+
+
 def test_mask_free_backward_70b_sampled():
     w = wl.WORKLOADS["bwd70b"]
     inp = wl.forward_inputs(w, C.DEV)

@@ -16,7 +16,9 @@ skip-path gradient.  Per case:
     same inputs, against the oracle from its bf16 shard sums;
   - the backward from the shards with the stored mask, and the mask-free one
     from the forward that stored none, every dResidual / dYpre element and the
-    parameter-gradient column sums;
+    parameter-gradient column sums; the forward and backward with the mask
+    stored one bit per element, bit for bit the byte-mask pair (h a multiple
+    of 32; other widths: the refusal);
   - the backward entered through g (t partial gradients reduce-scattered), or,
     for the shapes whose partial stages do not fit one SM's shared memory,
     the documented refusal with nothing written.
@@ -82,6 +84,7 @@ def test_case_list_spans_the_shape_space():
     assert any(w.t >= 11 for w in ws) and any(w.t == 1 for w in ws)
     assert {w.p for w in ws} >= {0.0, 0.9}
     assert any(c[1] for c in cases) and any(not c[1] for c in cases)
+    assert any(w.h % 32 == 0 for w in ws) and any(w.h % 32 for w in ws)   # bits, refusal
     for w in ws:
         assert w.h % 8 == 0 and 8 <= w.h <= 16384 and w.tokens * w.h <= ELEMS
         assert w.ragged or w.s % w.t == 0
@@ -141,6 +144,19 @@ def test_random_shape_every_entry_point_every_element(gpu, i):
     C.sp.check_device_status(C.DEV)
     C.check_bwd_rows(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], out, tokens)
     C.check_param_grads(w, fwd, inp["gamma"], bi["dy"], bi["dz_skip"], out)
+
+    # the mask stored one bit per element (h a multiple of 32): the byte mask
+    # packed, the rest bit for bit; other widths are refused
+    if w.h % 32 == 0:
+        fwd_k, bwd_k = C.run_bitmask_pair(w, inp, bi["dy"], bi["dz_skip"], w.n_gather,
+                                          n_gather_bwd, cu_seqlens=cu)
+        torch.cuda.synchronize()
+        C.sp.check_device_status(C.DEV)
+        C.assert_bitmask_pair_matches(w, fwd, out, fwd_k, bwd_k)
+    else:
+        with pytest.raises(C.sp.SpError):
+            C.run_bitmask_pair(w, inp, bi["dy"], bi["dz_skip"], w.n_gather, n_gather_bwd,
+                               cu_seqlens=cu)
 
     mf = C.alloc_bwd(w, n_gather_bwd)   # from the forward that stored no mask
     C.sp.sp_norm_bwd_philox(bi["dy"], nm["z"], nm["mean"], nm["rstd"], inp["gamma"],

@@ -347,3 +347,22 @@ def test_rs_norm_bwd_equals_norm_bwd_on_the_reduced_gradient():
     assert np.array_equal(a["dgamma"], b["dgamma"]) and np.array_equal(a["dbias"], b["dbias"])
     # (t-1) ranks x b rows x s/t tokens x h x 2 bytes
     assert a["rs_remote_bytes"] == [(w.t - 1) * 2 * (12 // 4) * 32 * 2] * w.t
+
+
+def test_pack_mask_bits_worked_bytes():
+    """Bytes worked out by hand from the layout's definition (channel 8j + e
+    in bit e of byte j), then numpy's own bit packing in little-endian bit
+    order as an independent routine, and the count of kept elements."""
+    rows = np.array([[1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1],
+                     [1, 1, 0, 1, 0, 0, 0, 0, 1, 1, 1, 1, 1, 1, 1, 1],
+                     [0, 0, 0, 0, 0, 0, 0, 0, 0, 1, 0, 1, 0, 1, 0, 1]], dtype=np.uint8)
+    got = ob.pack_mask_bits(rows)
+    assert got.dtype == np.uint8 and got.shape == (3, 2)
+    assert got.tolist() == [[0x01, 0x80], [0x0B, 0xFF], [0x00, 0xAA]]
+    rng = np.random.default_rng(3)
+    m = (rng.random((2, 5, 64)) < 0.7).astype(np.uint8)
+    packed = ob.pack_mask_bits(m)
+    assert np.array_equal(packed, np.packbits(m, axis=-1, bitorder="little"))
+    assert int(np.unpackbits(packed, axis=-1, bitorder="little").sum()) == int(m.sum())
+    with pytest.raises(ValueError):
+        ob.pack_mask_bits(np.ones((2, 12), dtype=np.uint8))
