@@ -313,11 +313,12 @@ class Step:
             if self.pipeline == "unfused":
                 self.sp.sp_reduce_scatter_seq(self.dy_parts, self.dy, cu_seqlens=self.cu)
             else:
-                self.sp.sp_rs_norm_bwd(
-                    self.dy_parts, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"],
-                    None, p=w.p, norm=w.norm, cu_seqlens=self.cu, dresidual=self.dres,
-                    dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
-                    dbias=self.dbias, workspace=self.ws)
+                rs_bwd = (self.sp.sp_rs_norm_bwd_bitmask if self.mask_mode == "bits"
+                          else self.sp.sp_rs_norm_bwd)
+                rs_bwd(self.dy_parts, self.z, self.mask, self.mean, self.rstd, self.inp["gamma"],
+                       None, p=w.p, norm=w.norm, cu_seqlens=self.cu, dresidual=self.dres,
+                       dgathered=self.dgat, dgamma=self.dgamma, dbeta=self.dbeta,
+                       dbias=self.dbias, workspace=self.ws)
                 return
         if self.mask_mode == "regen":
             self.sp.sp_norm_bwd_philox(
@@ -659,8 +660,8 @@ def run_ours(args):
     if args.norm is not None:
         w = w.with_(norm=args.norm, eps=1e-5 if args.norm == "layernorm" else 1e-6,
                     name=f"{w.name}-{args.norm}")
-    if args.mask != "stored" and args.bwd_entry == "g":
-        raise SystemExit("--mask regen / bits: the backward through g reads the byte mask")
+    if args.mask == "regen" and args.bwd_entry == "g":
+        raise SystemExit("--mask regen: the backward through g reads a stored mask")
     if args.mask == "bits" and args.pipeline != "fused":
         raise SystemExit("--mask bits: the fused forward only")
     kw = dict(n_gather=args.n_gather, pipeline=args.pipeline, mask=args.mask,
@@ -690,7 +691,7 @@ def run_ours(args):
     fb = ((fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
            unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm)) - mask_less) * w.tokens
     if args.bwd_entry == "g":
-        bb = bwd_g_bytes_per_token(w.t, w.h, args.n_gather, w.norm, fused) * w.tokens
+        bb = (bwd_g_bytes_per_token(w.t, w.h, args.n_gather, w.norm, fused) - mask_less) * w.tokens
     else:
         bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm) - mask_less) * w.tokens
     fwd_avg = statistics.mean(fwd_ms)

@@ -317,10 +317,11 @@ sp_status_t sp_norm_bwd_philox(const void* const* dy, const void* const* z,
                                void* stream);
 
 /*
- * sp_rs_norm_fwd_bitmask / sp_norm_bwd_bitmask -- the boundary with the
- * dropout mask stored one bit per element instead of one byte: the same keep
- * decisions, h / 8 bytes per token written, kept and read instead of h.
- * Arguments as for sp_rs_norm_fwd and sp_norm_bwd, except:
+ * sp_rs_norm_fwd_bitmask / sp_norm_bwd_bitmask / sp_rs_norm_bwd_bitmask --
+ * the boundary with the dropout mask stored one bit per element instead of
+ * one byte: the same keep decisions, h / 8 bytes per token written, kept and
+ * read instead of h.  Arguments as for sp_rs_norm_fwd, sp_norm_bwd and
+ * sp_rs_norm_bwd, except:
  *
  * mask_bits_out / mask_bits  [t]  (b, s_k, h / 8) u8, 16-byte aligned: byte
  *                j of a token row holds channels [8j, 8j + 8), bit e (value
@@ -330,8 +331,8 @@ sp_status_t sp_norm_bwd_philox(const void* const* dy, const void* const* z,
  *                before anything is enqueued
  *
  * The forward's other outputs are bit for bit those of sp_rs_norm_fwd; the
- * backward's are bit for bit those of sp_norm_bwd given the byte mask of the
- * same decisions (same launch shapes, same summation order).
+ * backwards' are bit for bit those of sp_norm_bwd and sp_rs_norm_bwd given the
+ * byte mask of the same decisions (same launch shapes, same summation order).
  */
 sp_status_t sp_rs_norm_fwd_bitmask(const void* const* partials, const void* const* residual,
                                    const void* bias, const void* gamma, const void* beta,
@@ -342,6 +343,15 @@ sp_status_t sp_rs_norm_fwd_bitmask(const void* const* partials, const void* cons
                                    float* const* mean_out, float* const* rstd_out,
                                    void* const* gathered, int32_t n_gather,
                                    int32_t* dev_status, void* stream);
+sp_status_t sp_rs_norm_bwd_bitmask(const void* const* dy_partials, const void* const* z,
+                                   const uint8_t* const* mask_bits, const float* const* mean,
+                                   const float* const* rstd, const void* gamma,
+                                   const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                                   int32_t t, double p, const int32_t* cu_seqlens,
+                                   int32_t n_seqs, sp_norm_t norm, void* const* dresidual,
+                                   void* const* dgathered, int32_t n_gather, float* dgamma,
+                                   float* dbeta, float* dbias, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, void* stream);
 sp_status_t sp_norm_bwd_bitmask(const void* const* dy, const void* const* z,
                                 const uint8_t* const* mask_bits, const float* const* mean,
                                 const float* const* rstd, const void* gamma,

@@ -67,6 +67,8 @@ def load():
         _u64, _u64, _vp, _i32, _i32, _PP, _PP, _PP, _PP, _PP, _vp, _vp]
     lib.sp_rs_norm_bwd.restype = _i32
     lib.sp_rs_norm_bwd.argtypes = list(lib.sp_norm_bwd.argtypes)
+    lib.sp_rs_norm_bwd_bitmask.restype = _i32
+    lib.sp_rs_norm_bwd_bitmask.argtypes = list(lib.sp_norm_bwd.argtypes)
     lib.sp_norm_bwd_bitmask.restype = _i32
     lib.sp_norm_bwd_bitmask.argtypes = list(lib.sp_norm_bwd.argtypes)
     lib.sp_rs_norm_fwd_bitmask.restype = _i32
@@ -362,6 +364,24 @@ def sp_rs_norm_bwd(dy_partials, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
                    dbeta=None, dbias=None, workspace, status=None):
     """Backward entered through g: reduce-scatter of the t partial gradients of
     the gathered input, fused into the norm / dropout backward."""
+    _rs_norm_bwd_call("sp_rs_norm_bwd", 1, dy_partials, z, mask, mean, rstd, gamma, dz_skip, p,
+                      cu_seqlens, norm, dresidual, dgathered, dgamma, dbeta, dbias, workspace,
+                      status)
+
+
+def sp_rs_norm_bwd_bitmask(dy_partials, z, mask_bits, mean, rstd, gamma, dz_skip=None, *, p,
+                           cu_seqlens=None, norm="layernorm", dresidual, dgathered,
+                           dgamma=None, dbeta=None, dbias=None, workspace, status=None):
+    """sp_rs_norm_bwd reading the mask stored one bit per element
+    (mask_bits[k]: (b, s_k, h / 8) uint8, bit e of byte j = channel 8j + e)."""
+    _rs_norm_bwd_call("sp_rs_norm_bwd_bitmask", 8, dy_partials, z, mask_bits, mean, rstd, gamma,
+                      dz_skip, p, cu_seqlens, norm, dresidual, dgathered, dgamma, dbeta, dbias,
+                      workspace, status)
+
+
+def _rs_norm_bwd_call(entry, mask_div, dy_partials, z, mask, mean, rstd, gamma, dz_skip, p,
+                      cu_seqlens, norm, dresidual, dgathered, dgamma, dbeta, dbias, workspace,
+                      status):
     lib = load()
     t = len(dy_partials)
     b, s, h = dy_partials[0].shape
@@ -373,7 +393,7 @@ def sp_rs_norm_bwd(dy_partials, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
         _need(dy_partials[r], (b, s, h), bf, dev, f"dy_partials[{r}]")
     for k in range(t):
         _need(z[k], (b, sizes[k], h), bf, dev, f"z[{k}]")
-        _need(mask[k], (b, sizes[k], h), torch.uint8, dev, f"mask[{k}]")
+        _need(mask[k], (b, sizes[k], h // mask_div), torch.uint8, dev, f"mask[{k}]")
         _need(rstd[k], (b, sizes[k]), torch.float32, dev, f"rstd[{k}]")
         if ln:
             _need(mean[k], (b, sizes[k]), torch.float32, dev, f"mean[{k}]")
@@ -390,7 +410,7 @@ def sp_rs_norm_bwd(dy_partials, z, mask, mean, rstd, gamma, dz_skip=None, *, p,
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    _check(lib.sp_rs_norm_bwd(
+    _check(getattr(lib, entry)(
         _ptr_array(dy_partials), _ptr_array(z), _ptr_array(mask),
         _ptr_array(mean) if ln else None, _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip),
         b, s, h, t, float(p), cu, n_seqs, NORMS[norm], _ptr_array(dresidual),

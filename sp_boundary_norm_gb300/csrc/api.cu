@@ -410,7 +410,7 @@ LaunchShape fwd_shard_shape_uncached(int64_t rows, int64_t h) {
 // row buffers (Z, mask, skip), the reduced dY in float32.  The row buffers are
 // double-buffered, which is safe while the prefetch reaches at most one row
 // ahead: stages - 1 <= chunks per row.
-LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip) {
+LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip, bool bits) {
   const int64_t nvec = h / 8;
   int threads, maxc;
   if (nvec <= 64) {
@@ -425,13 +425,14 @@ LaunchShape rs_bwd_shape_uncached(int64_t rows, int64_t h, int t, bool has_skip)
   }
   const size_t v16 = static_cast<size_t>(threads) * 16;
   const size_t stage = static_cast<size_t>(t) * v16;
-  const size_t rb_item = v16 + threads * 8 + (has_skip ? v16 : 0);
+  const size_t rb_item = static_cast<size_t>(rsbwd_rb_item_bytes(threads, has_skip, bits));
   const size_t fixed = 2 * maxc * rb_item + static_cast<size_t>(maxc) * 2 * v16 +
                        2 * 32 * sizeof(float2);
   static const int kOpts[] = {3, 2, 1};
   const int want = maxc + 1 < 3 ? maxc + 1 : 3;
-  return pick_shape(1, threads, maxc, rows, stage, fixed, kOpts, 3, want, 1,
-                    [&](int st) { return rs_bwd_kernel(threads, maxc, t, st); });
+  return pick_shape(1, threads, maxc, rows, stage, fixed, kOpts, 3, want, 1, [&](int st) {
+    return bits ? rs_bwd_bits_kernel(threads, maxc, t, st) : rs_bwd_kernel(threads, maxc, t, st);
+  });
 }
 
 // bulk: dYpre sent to the gathered copies by bulk copies from two shared
@@ -476,9 +477,9 @@ LaunchShape fwd_shard_shape(int64_t rows, int64_t h) {
   return cached_shape(1, rows, h, 1, 0, [&] { return fwd_shard_shape_uncached(rows, h); });
 }
 
-LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip) {
-  return cached_shape(2, rows, h, t, has_skip ? 1 : 0,
-                      [&] { return rs_bwd_shape_uncached(rows, h, t, has_skip); });
+LaunchShape rs_bwd_shape(int64_t rows, int64_t h, int t, bool has_skip, bool bits = false) {
+  return cached_shape(2, rows, h, t, (has_skip ? 1 : 0) | (bits ? 2 : 0),
+                      [&] { return rs_bwd_shape_uncached(rows, h, t, has_skip, bits); });
 }
 
 LaunchShape bwd_shape(int64_t rows, int64_t h, bool has_skip, bool regen = false,
@@ -859,8 +860,8 @@ size_t sp_norm_bwd_workspace_bytes(int64_t b, int64_t s, int64_t h, int32_t t, s
     if (ls.grid > grid) grid = ls.grid;
   }
   if (h <= 8192) {
-    for (int v = 0; v < 2; ++v) {
-      const LaunchShape ls = rs_bwd_shape(b * s, h, t, v != 0);
+    for (int v = 0; v < 4; ++v) {   // skip gradient or not; byte or bit mask
+      const LaunchShape ls = rs_bwd_shape(b * s, h, t, (v & 1) != 0, (v & 2) != 0 && h % 32 == 0);
       if (ls.grid > grid) grid = ls.grid;
     }
   }
@@ -997,15 +998,17 @@ static sp_status_t norm_bwd_common(
   return SP_OK;
 }
 
-sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
-                           const uint8_t* const* mask, const float* const* mean,
-                           const float* const* rstd, const void* gamma,
-                           const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
-                           int32_t t, double p, const int32_t* cu_seqlens, int32_t n_seqs,
-                           sp_norm_t norm, void* const* dresidual, void* const* dgathered,
-                           int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
-                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           void* stream) {
+// The backward entered through g, reading the mask as bytes or (bits) one
+// bit per element.
+static sp_status_t rs_norm_bwd_impl(const void* const* dy_partials, const void* const* z,
+                                    const uint8_t* const* mask, bool bits, const float* const* mean,
+                                    const float* const* rstd, const void* gamma,
+                                    const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                                    int32_t t, double p, const int32_t* cu_seqlens,
+                                    int32_t n_seqs, sp_norm_t norm, void* const* dresidual,
+                                    void* const* dgathered, int32_t n_gather, float* dgamma,
+                                    float* dbeta, float* dbias, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
   sp_status_t st;
   if (take_injected(&st)) return st;
   if ((st = check_shape(b, s, h, t, cu_seqlens, n_seqs)) != SP_OK) return st;
@@ -1044,7 +1047,7 @@ sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
   if (dev_status != nullptr && (reinterpret_cast<uintptr_t>(dev_status) & 3u))
     return fail(SP_ERR_MISALIGNED, "dev_status misaligned");
   const bool has_skip = dz_skip != nullptr;
-  const LaunchShape ls = rs_bwd_shape(rows, h, t, has_skip);
+  const LaunchShape ls = rs_bwd_shape(rows, h, t, has_skip, bits);
   g_last_shape[1] = ls;
   const size_t need = static_cast<size_t>(ls.grid) * 3 * h * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need)
@@ -1057,7 +1060,7 @@ sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
   for (int k = 0; k < t; ++k) {
     const size_t n = static_cast<size_t>(shard_rows(map, k));
     rg.add(z[k], n * h * 2, false, "z", k);
-    rg.add(mask[k], n * h, false, "mask", k);
+    rg.add(mask[k], bits ? n * h / 8 : n * h, false, "mask", k);
     rg.add(rstd[k], n * 4, false, "rstd", k);
     if (ln) rg.add(mean[k], n * 4, false, "mean", k);
     if (has_skip) rg.add(dz_skip[k], n * h * 2, false, "dz_skip", k);
@@ -1094,7 +1097,9 @@ sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
   P.ws = static_cast<float*>(workspace);
   P.status = dev_status;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch(rs_bwd_kernel(ls.threads, ls.maxc, t, ls.stages), ls, &P, cs);
+  cudaError_t e = launch(bits ? rs_bwd_bits_kernel(ls.threads, ls.maxc, t, ls.stages)
+                             : rs_bwd_kernel(ls.threads, ls.maxc, t, ls.stages),
+                        ls, &P, cs);
   if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_bwd launch");
   if (dgamma || (dbeta && ln) || dbias) {
     ParamReduceParams R{};
@@ -1108,6 +1113,37 @@ sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
     if (e != cudaSuccess) return fail_cuda(e, "sp_rs_norm_bwd parameter reduce launch");
   }
   return SP_OK;
+}
+
+sp_status_t sp_rs_norm_bwd(const void* const* dy_partials, const void* const* z,
+                           const uint8_t* const* mask, const float* const* mean,
+                           const float* const* rstd, const void* gamma,
+                           const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                           int32_t t, double p, const int32_t* cu_seqlens, int32_t n_seqs,
+                           sp_norm_t norm, void* const* dresidual, void* const* dgathered,
+                           int32_t n_gather, float* dgamma, float* dbeta, float* dbias,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  return rs_norm_bwd_impl(dy_partials, z, mask, false, mean, rstd, gamma, dz_skip, b, s, h, t,
+                          p, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma,
+                          dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
+}
+
+sp_status_t sp_rs_norm_bwd_bitmask(const void* const* dy_partials, const void* const* z,
+                                   const uint8_t* const* mask_bits, const float* const* mean,
+                                   const float* const* rstd, const void* gamma,
+                                   const void* const* dz_skip, int64_t b, int64_t s, int64_t h,
+                                   int32_t t, double p, const int32_t* cu_seqlens,
+                                   int32_t n_seqs, sp_norm_t norm, void* const* dresidual,
+                                   void* const* dgathered, int32_t n_gather, float* dgamma,
+                                   float* dbeta, float* dbias, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (h % 32 != 0)
+    return fail(SP_ERR_UNSUPPORTED, "bit-packed mask: h = %lld must be a multiple of 32",
+                (long long)h);
+  return rs_norm_bwd_impl(dy_partials, z, mask_bits, true, mean, rstd, gamma, dz_skip, b, s, h,
+                          t, p, cu_seqlens, n_seqs, norm, dresidual, dgathered, n_gather, dgamma,
+                          dbeta, dbias, workspace, workspace_bytes, dev_status, stream);
 }
 
 sp_status_t sp_norm_bwd(const void* const* dy, const void* const* z, const uint8_t* const* mask,

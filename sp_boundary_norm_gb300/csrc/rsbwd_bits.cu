@@ -1,0 +1,11 @@
+// Instantiations of the backward entered through g (rsbwd_kernel.cuh) with the
+// dropout mask stored one bit per element.
+#include "rsbwd_kernel.cuh"
+
+namespace spb {
+
+const void* rs_bwd_bits_kernel(int threads, int maxc, int t, int stages) {
+  return rs_bwd_any<true>(threads, maxc, t, stages);
+}
+
+}  // namespace spb

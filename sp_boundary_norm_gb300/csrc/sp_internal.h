@@ -46,6 +46,17 @@ __host__ __device__ constexpr int bwd_item_bytes(int nthr, bool has_skip, bool r
   return bwd_item_skip_offset(nthr, regen, bits) + (has_skip ? nthr * 16 : 0);
 }
 
+// The backward entered through g keeps each row's Z, mask and optional skip
+// gradient in a row buffer of MAXC such items, shared by its kernel and the
+// host: Z (16 bytes per thread), the mask (8 bytes per thread as bytes, one
+// byte per thread as bits), the skip gradient (16 bytes per thread).
+__host__ __device__ constexpr int rsbwd_rb_skip_offset(int nthr, bool bits) {
+  return nthr * 16 + (bits ? nthr : nthr * 8);
+}
+__host__ __device__ constexpr int rsbwd_rb_item_bytes(int nthr, bool has_skip, bool bits) {
+  return rsbwd_rb_skip_offset(nthr, bits) + (has_skip ? nthr * 16 : 0);
+}
+
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
@@ -191,6 +202,8 @@ const void* bwd_bits_kernel(int threads, int maxc, int ring);
 // Backward entered through g (reduce-scatter of t partial gradients fused):
 // (threads, chunks per row, ranks t, chunk stages).
 const void* rs_bwd_kernel(int threads, int maxc, int t, int stages);
+// The same reading the mask stored one bit per element.
+const void* rs_bwd_bits_kernel(int threads, int maxc, int t, int stages);
 
 // Workspace bytes of one sp_norm_bwd call (stored mask) of `rows` tokens of
 // width h (0 for shapes outside the limits): its own launch grid, not the

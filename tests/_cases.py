@@ -207,6 +207,29 @@ def assert_bitmask_pair_matches(w, fwd_bytes, bwd_bytes, fwd_bits, bwd_bits):
         assert bits_equal(bwd_bytes[key], bwd_bits[key]), key
 
 
+def oracle_mask_bits(byte_masks):
+    """The oracle's packing of device byte masks, as device tensors."""
+    return [torch.from_numpy(ob.pack_mask_bits(m.cpu().numpy())).to(DEV) for m in byte_masks]
+
+
+def run_rs_bwd_bitmask(w, fwd, inp, parts, dz_skip, mask_bits, n_gather, cu_seqlens=None):
+    out = alloc_bwd(w, n_gather)
+    sp.sp_rs_norm_bwd_bitmask(parts, fwd["z"], mask_bits, fwd["mean"], fwd["rstd"], inp["gamma"],
+                              dz_skip, p=w.p, norm=w.norm, cu_seqlens=cu_seqlens,
+                              dresidual=out["dres"], dgathered=out["dgat"], dgamma=out["dgamma"],
+                              dbeta=out["dbeta"] if w.norm == "layernorm" else None,
+                              dbias=out["dbias"], workspace=out["ws"])
+    return out
+
+
+def assert_bwd_outputs_equal(w, a, b):
+    for key in ("dres", "dgat"):
+        for x, y in zip(a[key], b[key]):
+            assert bits_equal(x, y), key
+    for key in ("dgamma", "dbias") + (("dbeta",) if w.norm == "layernorm" else ()):
+        assert bits_equal(a[key], b[key]), key
+
+
 def token_shard(w, g):
     """(shard k, local row) of global token g for b == 1 or dense b > 1."""
     bi, si = divmod(int(g), w.s)

@@ -164,3 +164,24 @@ def test_bit_mask_pair_full_size_equals_byte_mask_pair(name):
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     C.assert_bitmask_pair_matches(w, fwd_b, bwd_b, fwd_k, bwd_k)
+
+
+def test_rs_norm_bwd_bit_mask_full_size_equals_byte_mask():
+    """The backward entered through g at the 70B shape, reading the bit-packed
+    mask, equals the byte-mask call (checked against the oracle above) bit for
+    bit."""
+    w = wl.WORKLOADS["bwd70b"]
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(97, C.DEV)
+    parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=C.DEV) * 0.35).to(torch.bfloat16)
+             for _ in range(w.t)]
+    ref = C.alloc_bwd(w, 1)
+    C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                        None, p=w.p, norm=w.norm, dresidual=ref["dres"], dgathered=ref["dgat"],
+                        dgamma=ref["dgamma"], dbeta=ref["dbeta"], dbias=ref["dbias"],
+                        workspace=ref["ws"])
+    got = C.run_rs_bwd_bitmask(w, fwd, inp, parts, None, C.oracle_mask_bits(fwd["mask"]), 1)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.assert_bwd_outputs_equal(w, ref, got)

@@ -1006,6 +1006,37 @@ def test_rs_norm_bwd_70b_sampled():
     _rs_bwd_check(w, fwd, inp, parts, None, out, tokens=tokens)
 
 
+@pytest.mark.parametrize("variant", [dict(), dict(norm="rmsnorm", eps=1e-6), dict(t=3, s=48),
+                                     dict(b=2, s=40, t=4), dict(h=5120, s=24), dict(h=96, s=16),
+                                     dict(t=16, s=32), dict(n_gather=3), dict(p=0.0),
+                                     dict(seqlens=(5, 17, 3, 40, 1, 9), s=75, t=4, h=256)])
+@pytest.mark.parametrize("with_skip", [False, True])
+def test_rs_norm_bwd_bit_mask_equals_byte_mask(variant, with_skip):
+    """The backward entered through g reading the mask as bits (the oracle's
+    packing of the stored byte mask) gives every output of the byte-mask call
+    bit for bit."""
+    w = wl.Workload("rsbits", t=2, b=1, s=64, h=512, draw_seed=83).with_(**variant)
+    cu = torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=0)
+    gen = wl.make_generator(96, C.DEV)
+    parts = [(torch.randn((w.b, w.s, w.h), generator=gen, device=C.DEV) * 0.5).to(torch.bfloat16)
+             for _ in range(w.t)]
+    skip = wl.backward_inputs(w, C.DEV, with_skip=True)["dz_skip"] if with_skip else None
+    ng = w.n_gather
+    ref = C.alloc_bwd(w, ng)
+    C.sp.sp_rs_norm_bwd(parts, fwd["z"], fwd["mask"], fwd["mean"], fwd["rstd"], inp["gamma"],
+                        skip, p=w.p, norm=w.norm, cu_seqlens=cu, dresidual=ref["dres"],
+                        dgathered=ref["dgat"], dgamma=ref["dgamma"],
+                        dbeta=ref["dbeta"] if w.norm == "layernorm" else None,
+                        dbias=ref["dbias"], workspace=ref["ws"])
+    got = C.run_rs_bwd_bitmask(w, fwd, inp, parts, skip, C.oracle_mask_bits(fwd["mask"]), ng,
+                               cu_seqlens=cu)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.assert_bwd_outputs_equal(w, ref, got)
+
+
 @pytest.mark.parametrize("t,h,skip", [(2, 16384, False), (16, 8192, True)])
 def test_rs_norm_bwd_rejects_shapes_it_cannot_run(t, h, skip):
     """h above 8192, and t = 16 at h = 8192 with a skip gradient (the t partial

@@ -196,3 +196,9 @@ def test_random_shape_every_entry_point_every_element(gpu, i):
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     C.rs_bwd_check(w, fwd, inp, parts, bi["dz_skip"], rs)
+    if w.h % 32 == 0:   # the same call reading the bit-packed mask: the same bits
+        rk = C.run_rs_bwd_bitmask(w, fwd, inp, parts, bi["dz_skip"],
+                                  C.oracle_mask_bits(fwd["mask"]), n_gather_bwd, cu_seqlens=cu)
+        torch.cuda.synchronize()
+        C.sp.check_device_status(C.DEV)
+        C.assert_bwd_outputs_equal(w, rs, rk)
