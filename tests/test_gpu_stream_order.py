@@ -52,9 +52,17 @@ def _alloc_set(w, dev):
         # the unfused forward: reduce-scatter, norm on the shards, all-gather
         "y": shard(torch.bfloat16), "z2": shard(torch.bfloat16), "mask2": shard(torch.uint8),
         "mean2": stats(), "rstd2": stats(), "o2": shard(torch.bfloat16), "g2": full(1),
+        # the bit-mask forward and backward
+        "zk": shard(torch.bfloat16), "bits": [e((w.b, n, w.h // 8), torch.uint8) for n in sizes],
+        "meank": stats(), "rstdk": stats(), "gk": full(1), "dk": shard(torch.bfloat16),
+        "dgk": full(1), "dgammak": vec(), "dbetak": vec(), "dbiask": vec(),
+        # the forward storing no mask and the mask-free backward
+        "zn": shard(torch.bfloat16), "meann": stats(), "rstdn": stats(), "gn": full(1),
+        "dn": shard(torch.bfloat16), "dgn": full(1), "dgamman": vec(), "dbetan": vec(),
+        "dbiasn": vec(),
     }
     if w.norm != "layernorm":   # RMSNorm has no mean and no beta
-        for key in ("mean", "mean2", "dbeta", "dbeta2"):
+        for key in ("mean", "mean2", "dbeta", "dbeta2", "meank", "dbetak", "meann", "dbetan"):
             del st[key]
     return st
 
@@ -80,7 +88,9 @@ def _chain(w, inp, dy, cu, sets, ws, sync):
     """STEPS steps; step i reads set (i - 1) % 2 (the inputs for i = 0) and
     writes set i % 2.  Per step: fused forward -> backward from the shards
     (+ parameter reduce) -> backward through g (+ parameter reduce) ->
-    reduce-scatter -> shard norm -> all-gather."""
+    reduce-scatter -> shard norm -> all-gather -> bit-mask forward ->
+    bit-mask backward (+ reduce) -> forward storing no mask -> mask-free
+    backward (+ reduce); each reads what the call before it wrote."""
     after = (lambda: torch.cuda.synchronize()) if sync else (lambda: None)
     prev = {"g": inp["partials"], "z2": inp["residual"], "d2": dy}
     for i in range(STEPS):
@@ -110,6 +120,30 @@ def _chain(w, inp, dy, cu, sets, ws, sync):
                              rstd_out=cur["rstd2"], o_shards=cur["o2"])
         after()
         sp.sp_allgather_seq(cur["o2"], cur["g2"], s=w.s, cu_seqlens=cu)
+        after()
+        sp.sp_rs_norm_fwd_bitmask([cur["g2"][0]] * w.t, cur["z2"], inp["bias"], inp["gamma"],
+                                  inp["beta"], eps=w.eps, p=w.p, seed=w.seed,
+                                  offset=w.offset + 200 + i, norm=w.norm, cu_seqlens=cu,
+                                  z_out=cur["zk"], mask_bits_out=cur["bits"],
+                                  mean_out=cur.get("meank"), rstd_out=cur["rstdk"],
+                                  gathered=cur["gk"])
+        after()
+        sp.sp_norm_bwd_bitmask(cur["d2"], cur["zk"], cur["bits"], cur.get("meank"),
+                               cur["rstdk"], inp["gamma"], None, s=w.s, p=w.p, norm=w.norm,
+                               cu_seqlens=cu, dresidual=cur["dk"], dgathered=cur["dgk"],
+                               dgamma=cur["dgammak"], dbeta=cur.get("dbetak"),
+                               dbias=cur["dbiask"], workspace=ws)
+        after()
+        sp.sp_rs_norm_fwd([cur["gk"][0]] * w.t, cur["dk"], inp["bias"], inp["gamma"],
+                          inp["beta"], eps=w.eps, p=w.p, seed=w.seed, offset=w.offset + 300 + i,
+                          norm=w.norm, cu_seqlens=cu, z_out=cur["zn"], mask_out=None,
+                          mean_out=cur.get("meann"), rstd_out=cur["rstdn"], gathered=cur["gn"])
+        after()
+        sp.sp_norm_bwd_philox(cur["dk"], cur["zn"], cur.get("meann"), cur["rstdn"], inp["gamma"],
+                              None, s=w.s, p=w.p, seed=w.seed, offset=w.offset + 300 + i,
+                              norm=w.norm, cu_seqlens=cu, dresidual=cur["dn"],
+                              dgathered=cur["dgn"], dgamma=cur["dgamman"],
+                              dbeta=cur.get("dbetan"), dbias=cur["dbiasn"], workspace=ws)
         after()
         prev = cur
 
