@@ -78,6 +78,21 @@ def bwd_bytes_per_token(h, n_gather, norm="layernorm", skip=False):
     return 2 * h + 2 * h + h + stats + (2 * h if skip else 0) + 2 * h + 2 * h * n_gather
 
 
+def step_bytes_per_token(w, n_gather, pipeline="fused", mask="stored", bwd_entry="shard"):
+    """(forward, backward) algorithmic bytes per token of one bench step.  The
+    mask moves h bytes per token as bytes, h / 8 as bits ("bits") and none in
+    the mask-free step ("regen"), in each direction."""
+    fused = pipeline == "fused"
+    mask_less = {"stored": 0, "regen": w.h, "bits": w.h - w.h // 8}[mask]
+    fwd = (fwd_bytes_per_token(w.t, w.h, n_gather, w.norm) if fused else
+           unfused_fwd_bytes_per_token(w.t, w.h, n_gather, w.norm)) - mask_less
+    if bwd_entry == "g":
+        bwd = bwd_g_bytes_per_token(w.t, w.h, n_gather, w.norm, fused) - mask_less
+    else:
+        bwd = bwd_bytes_per_token(w.h, n_gather, w.norm) - mask_less
+    return fwd, bwd
+
+
 def launches_per_step(fused, n_gather, bwd_entry):
     """Kernels of this library one step launches.  Forward: the fused kernel,
     or reduce-scatter + shard norm (+ all-gather).  Backward: the norm
@@ -687,13 +702,8 @@ def run_ours(args):
     tokens = w.tokens * args.steps * world
     value = tokens / (total_ms / 1e3)
     fused = args.pipeline == "fused"
-    mask_less = {"stored": 0, "regen": w.h, "bits": w.h - w.h // 8}[args.mask]
-    fb = ((fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm) if fused else
-           unfused_fwd_bytes_per_token(w.t, w.h, args.n_gather, w.norm)) - mask_less) * w.tokens
-    if args.bwd_entry == "g":
-        bb = (bwd_g_bytes_per_token(w.t, w.h, args.n_gather, w.norm, fused) - mask_less) * w.tokens
-    else:
-        bb = (bwd_bytes_per_token(w.h, args.n_gather, w.norm) - mask_less) * w.tokens
+    fpt, bpt = step_bytes_per_token(w, args.n_gather, args.pipeline, args.mask, args.bwd_entry)
+    fb, bb = fpt * w.tokens, bpt * w.tokens
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     peak, peak_kind = measured_peak()

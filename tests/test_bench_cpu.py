@@ -57,3 +57,15 @@ def test_bucketed_step_covers_the_batch(lib):
     assert len(step.outputs()) == len(buckets) * len(one.outputs())
     assert sum(x.numel() for x in step.inputs()) == \
         (w.t * w.s * w.h) + 2 * (w.s * w.h)   # partials, residual, dY
+
+
+@pytest.mark.parametrize("mask,entry,fwd,bwd", [
+    ("stored", "shard", 23 * 8192 + 8, 9 * 8192 + 8),
+    ("bits", "shard", 22 * 8192 + 1024 + 8, 8 * 8192 + 1024 + 8),   # h / 8 bytes of mask
+    ("regen", "shard", 22 * 8192 + 8, 8 * 8192 + 8),                # no mask at all
+    ("stored", "g", 23 * 8192 + 8, 23 * 8192 + 8),   # t = 8 partial gradients read
+    ("bits", "g", 22 * 8192 + 1024 + 8, 22 * 8192 + 1024 + 8),
+])
+def test_step_bytes_of_each_mask_mode(mask, entry, fwd, bwd):
+    w = wl.WORKLOADS["70b"]
+    assert bench.step_bytes_per_token(w, 1, "fused", mask, entry) == (fwd, bwd)
