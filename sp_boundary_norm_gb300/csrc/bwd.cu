@@ -11,7 +11,8 @@
 // token rows per block, chunks of 8*T channels with thread i owning channels
 // [8i, 8i+8) of each chunk.  Each thread stages its own pieces of dY, Z, the
 // mask (and the optional skip-path gradient) of whole rows with cp.async into
-// a ring of RING rows in shared memory, RING - 1 rows ahead; the row's
+// a ring of RING rows in shared memory, RING - 1 rows ahead (a bit-packed
+// mask is staged by 8 lanes per warp for the whole warp); the row's
 // statistics are loaded when it is staged and wait in registers.  The two
 // passes a row needs (the row sums mean(dxh) and mean(dxh * x_hat), then the
 // gradients) both read the row from there.  The two sums are reduced

@@ -11,7 +11,7 @@
 // (t times the bytes of one row) in the first pass only, while the second pass
 // needs Z, the mask and dY again.  So there are two staging areas in shared
 // memory, both filled per thread with cp.async (each thread reads back only
-// what it copied):
+// what it copied, except the bit-packed mask's bytes, see BITS below):
 //   - a ring of STAGES chunk stages for the t partial pieces (streamed through
 //     the first pass);
 //   - two row buffers (the current row, the next) for Z, the mask and the
