@@ -923,6 +923,28 @@ def test_bit_mask_refuses_widths_not_a_multiple_of_32(h):
     assert all(bool((x == 3.0).all()) for x in out["dres"])
 
 
+@pytest.mark.parametrize("shape,ring", [((256, 4), 2), ((256, 4), 3), ((512, 2), 1),
+                                        ((512, 2), 2), ((128, 4), 2)])
+def test_bit_mask_backward_forced_shapes(bwd_shape, shape, ring):
+    """The bit-mask backward in launch shapes other than the default (the
+    tensor-memory shapes, shallower rings): with the same shape forced for
+    both, it gives the byte-mask backward's outputs bit for bit."""
+    bwd_shape(*shape, ring=ring)
+    w = wl.Workload("bmf", t=4, b=1, s=96, h=8192 if shape[0] >= 256 else 4096, draw_seed=76)
+    inp = wl.forward_inputs(w, C.DEV)
+    # (three staged rows of the tensor-memory shape fit beside a second block
+    # only without the skip gradient)
+    bi = wl.backward_inputs(w, C.DEV, with_skip=ring < 3)
+    fwd_b = C.run_fwd(w, inp, n_gather=1)
+    bwd_b = C.run_bwd(w, fwd_b, inp["gamma"], bi["dy"], bi["dz_skip"], n_gather=1)
+    fwd_k, bwd_k = C.run_bitmask_pair(w, inp, bi["dy"], bi["dz_skip"], 1, 1)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    got = C.sp.sp_debug_last_shape(1)
+    assert (got["threads"], got["chunks"], got["stages"]) == (shape[0], shape[1], ring)
+    C.assert_bitmask_pair_matches(w, fwd_b, bwd_b, fwd_k, bwd_k)
+
+
 def test_mask_free_backward_70b_sampled():
     w = wl.WORKLOADS["bwd70b"]
     inp = wl.forward_inputs(w, C.DEV)
