@@ -5,14 +5,17 @@
  * one forward (sp_rs_norm_fwd) and the backward that reads its saved Z,
  * mask and statistics (sp_norm_bwd), on the legacy default stream.
  *
- * usage: sp_roundtrip IN OUT t b s h norm p seed offset eps
+ * usage: sp_roundtrip IN OUT t b s h norm p seed offset eps [bits]
+ *
+ * With the last argument "bits" the pair is sp_rs_norm_fwd_bitmask /
+ * sp_norm_bwd_bitmask and the masks are (b, s_k, h / 8) bit-packed bytes.
  *
  * IN holds, as raw little-endian arrays in this order: the t partials
  * (b, s, h) bf16; the t residual shards (b, s_k, h) bf16; bias, gamma,
  * beta (h) bf16; the t dY shards (b, s_k, h) bf16.  Shard k is tokens
  * [o_k, o_{k+1}) of every batch row, o_k = floor(k * s / t).
- * OUT receives: the t Z shards (bf16), the t masks (u8), the t mean rows
- * (f32, LayerNorm only), the t rstd rows (f32), one gathered copy of O
+ * OUT receives: the t Z shards (bf16), the t masks (u8, bytes or bits), the
+ * t mean rows (f32, LayerNorm only), the t rstd rows (f32), one gathered copy of O
  * (b, s, h) bf16, the t dResidual shards (bf16), one dYpre copy (b, s, h)
  * bf16, dgamma, dbeta (LayerNorm only), dbias (h) f32, and the int32
  * device status word.  Exit status 0 on success, 1 on any error (with the
@@ -74,10 +77,11 @@ static int write_from_device(FILE* f, const void* d, size_t bytes) {
 }
 
 int main(int argc, char** argv) {
-  if (argc != 12) {
-    fprintf(stderr, "usage: %s IN OUT t b s h norm p seed offset eps\n", argv[0]);
+  if (argc != 12 && argc != 13) {
+    fprintf(stderr, "usage: %s IN OUT t b s h norm p seed offset eps [bits]\n", argv[0]);
     return 1;
   }
+  const int bits = argc == 13 && strcmp(argv[12], "bits") == 0;
   const int32_t t = (int32_t)atoi(argv[3]);
   const int64_t b = strtoll(argv[4], NULL, 10), s = strtoll(argv[5], NULL, 10);
   const int64_t h = strtoll(argv[6], NULL, 10);
@@ -122,9 +126,10 @@ int main(int argc, char** argv) {
   float* mean[MAXT];
   float* rstd[MAXT];
   void* dres[MAXT];
+  const size_t mask_row = bits ? (size_t)h / 8 : (size_t)h;   /* mask bytes per token */
   for (int k = 0; k < t; ++k) {
     z[k] = dev_alloc(rows_k[k] * h * 2);
-    mask[k] = (uint8_t*)dev_alloc(rows_k[k] * h);
+    mask[k] = (uint8_t*)dev_alloc(rows_k[k] * mask_row);
     mean[k] = (float*)dev_alloc(rows_k[k] * 4);
     rstd[k] = (float*)dev_alloc(rows_k[k] * 4);
     dres[k] = dev_alloc(rows_k[k] * h * 2);
@@ -141,19 +146,17 @@ int main(int argc, char** argv) {
   if (!gathered || !dgat || !dgamma || !dbeta || !dbias || !status || !ws) return 1;
   if (!cuda_ok(cudaMemset(status, 0, 4), "cudaMemset")) return 1;
 
-  if (!sp_ok(sp_rs_norm_fwd(partials, residual, bias, gamma, ln ? beta : NULL, b, s, h, t, eps,
-                            p, seed, offset, NULL, 0, norm, (void* const*)z,
-                            (uint8_t* const*)mask, ln ? (float* const*)mean : NULL,
-                            (float* const*)rstd, (void* const*)&gathered, 1, status, NULL),
-             "sp_rs_norm_fwd"))
-    return 1;
-  if (!sp_ok(sp_norm_bwd(dy, (const void* const*)z, (const uint8_t* const*)mask,
-                         ln ? (const float* const*)mean : NULL, (const float* const*)rstd,
-                         gamma, NULL, b, s, h, t, p, NULL, 0, norm, (void* const*)dres,
-                         (void* const*)&dgat, 1, dgamma, ln ? dbeta : NULL, dbias, ws, ws_bytes,
-                         status, NULL),
-             "sp_norm_bwd"))
-    return 1;
+  sp_status_t st = (bits ? sp_rs_norm_fwd_bitmask : sp_rs_norm_fwd)(
+      partials, residual, bias, gamma, ln ? beta : NULL, b, s, h, t, eps, p, seed, offset, NULL,
+      0, norm, (void* const*)z, (uint8_t* const*)mask, ln ? (float* const*)mean : NULL,
+      (float* const*)rstd, (void* const*)&gathered, 1, status, NULL);
+  if (!sp_ok(st, "forward")) return 1;
+  st = (bits ? sp_norm_bwd_bitmask : sp_norm_bwd)(
+      dy, (const void* const*)z, (const uint8_t* const*)mask,
+      ln ? (const float* const*)mean : NULL, (const float* const*)rstd, gamma, NULL, b, s, h, t,
+      p, NULL, 0, norm, (void* const*)dres, (void* const*)&dgat, 1, dgamma, ln ? dbeta : NULL,
+      dbias, ws, ws_bytes, status, NULL);
+  if (!sp_ok(st, "backward")) return 1;
   if (!cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return 1;
 
   FILE* out = fopen(argv[2], "wb");
@@ -163,7 +166,7 @@ int main(int argc, char** argv) {
   }
   int ok = 1;
   for (int k = 0; k < t; ++k) ok = ok && write_from_device(out, z[k], rows_k[k] * h * 2);
-  for (int k = 0; k < t; ++k) ok = ok && write_from_device(out, mask[k], rows_k[k] * h);
+  for (int k = 0; k < t; ++k) ok = ok && write_from_device(out, mask[k], rows_k[k] * mask_row);
   if (ln)
     for (int k = 0; k < t; ++k) ok = ok && write_from_device(out, mean[k], rows_k[k] * 4);
   for (int k = 0; k < t; ++k) ok = ok && write_from_device(out, rstd[k], rows_k[k] * 4);

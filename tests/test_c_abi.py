@@ -74,11 +74,13 @@ def _bits(x):
 
 @needs_cc
 @pytest.mark.gpu
-@pytest.mark.parametrize("variant", [
-    dict(),
-    dict(t=3, b=2, s=48, h=520, norm="rmsnorm", eps=1e-6, p=0.3, seed=2**40 + 9, offset=77),
+@pytest.mark.parametrize("variant,bits", [
+    (dict(), False),
+    (dict(t=3, b=2, s=48, h=520, norm="rmsnorm", eps=1e-6, p=0.3, seed=2**40 + 9, offset=77),
+     False),
+    (dict(t=4, b=1, s=64, h=544, p=0.2, seed=5, offset=3), True),   # the bit-packed mask
 ])
-def test_c_consumer_gives_the_bits_of_the_binding(lib, tmp_path, variant):
+def test_c_consumer_gives_the_bits_of_the_binding(lib, tmp_path, variant, bits):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     C = pytest.importorskip("_cases")
@@ -98,12 +100,16 @@ def test_c_consumer_gives_the_bits_of_the_binding(lib, tmp_path, variant):
     exe = _compile(tmp_path)
     res = subprocess.run([exe, str(tmp_path / "in.bin"), str(tmp_path / "out.bin"), str(w.t),
                           str(w.b), str(w.s), str(w.h), w.norm, repr(w.p), str(w.seed),
-                          str(w.offset), repr(w.eps)], capture_output=True, text=True,
-                         timeout=120)
+                          str(w.offset), repr(w.eps)] + (["bits"] if bits else []),
+                         capture_output=True, text=True, timeout=120)
     assert res.returncode == 0, res.stdout + res.stderr
 
-    fwd = C.run_fwd(w, inp, n_gather=1)
-    bwd = C.run_bwd(w, fwd, inp["gamma"], dy, None, n_gather=1)
+    if bits:
+        fwd, bwd = C.run_bitmask_pair(w, inp, dy, None, 1, 1)
+        fwd["mask"] = fwd["mask_bits"]
+    else:
+        fwd = C.run_fwd(w, inp, n_gather=1)
+        bwd = C.run_bwd(w, fwd, inp["gamma"], dy, None, n_gather=1)
     torch.cuda.synchronize()
     C.sp.check_device_status(dev)
     want = b"".join(
