@@ -162,3 +162,27 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         binding.load()
+
+
+def test_bit_mask_entry_points_validate_on_the_host():
+    """The bit-packed mask needs h % 32 == 0 and a mask array; both are
+    refused before anything is enqueued, by the forward and both backwards."""
+    from sp_boundary_norm_gb300 import binding
+    lib = binding.load()
+    args = _fwd_args(h=520)
+    assert lib.sp_rs_norm_fwd_bitmask(*args) == 3             # SP_ERR_UNSUPPORTED
+    assert b"multiple of 32" in lib.sp_last_error()
+    args = _fwd_args(h=512)
+    args[17] = None                                           # the mask_bits_out array
+    assert lib.sp_rs_norm_fwd_bitmask(*args) == 1             # SP_ERR_INVALID_ARG
+    assert b"mask_bits_out" in lib.sp_last_error()
+    arr = _arr([FAKE, FAKE + (1 << 30)])
+    for fn in (lib.sp_norm_bwd_bitmask, lib.sp_rs_norm_bwd_bitmask):
+        r = fn(arr, arr, arr, arr, arr, ctypes.c_void_p(FAKE), None, 1, 8, 520, 2, 0.1, None, 0,
+               0, arr, arr, 1, None, None, None, None, 0, None, None)
+        assert r == 3 and b"multiple of 32" in lib.sp_last_error()
+    # the byte-mask forward accepts a NULL mask array (nothing stored): it
+    # gets past the mask check and stops at the next invalid argument
+    args = _fwd_args(h=512, p=1.5)
+    args[17] = None
+    assert lib.sp_rs_norm_fwd(*args) == 1 and b"p = " in lib.sp_last_error()
