@@ -359,23 +359,46 @@ class Step:
 
 class BucketedStep:
     """One step of a packed batch bucketed by length: the boundary's forward
-    and backward on every bucket in turn (each bucket a packed batch of its
-    own with its cu_seqlens), covering the same sequences as the whole batch."""
+    and backward on every bucket (each bucket a packed batch of its own with
+    its cu_seqlens), covering the same sequences as the whole batch.  The
+    buckets share no buffer, so each runs on a stream of its own, forked from
+    and joined back to the caller's stream (one bucket's blocks start while
+    another's last blocks finish); serial=True runs them in turn instead."""
 
-    def __init__(self, w, device, buckets, **kw):
+    def __init__(self, w, device, buckets, serial=False, **kw):
         self.buckets = buckets
+        self.device = device
         self.steps = [Step(w.with_(name=f"{w.name}-bucket{i}", s=b.tokens,
                                    seqlens=tuple(b.lengths), draw_seed=w.draw_seed + 100 + i),
                            device, **kw) for i, b in enumerate(buckets)]
         self.sp = self.steps[0].sp
+        self.streams = (None if serial or device.type != "cuda" else
+                        [torch.cuda.Stream(device) for _ in buckets])
+
+    def _each(self, call):
+        if self.streams is None:
+            for st in self.steps:
+                call(st)
+            return
+        main = torch.cuda.current_stream(self.device)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        joins = []
+        for st, stream in zip(self.steps, self.streams):
+            stream.wait_event(fork)
+            with torch.cuda.stream(stream):
+                call(st)
+                done = torch.cuda.Event()
+                done.record(stream)
+            joins.append(done)
+        for done in joins:
+            main.wait_event(done)
 
     def fwd(self):
-        for st in self.steps:
-            st.fwd()
+        self._each(lambda st: st.fwd())
 
     def bwd(self):
-        for st in self.steps:
-            st.bwd()
+        self._each(lambda st: st.bwd())
 
     def inputs(self):
         return [x for st in self.steps for x in st.inputs()]
