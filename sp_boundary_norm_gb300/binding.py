@@ -143,8 +143,11 @@ _status = {}
 
 
 def device_status(device):
-    """The binding's device status word for ``device`` (an int32 tensor)."""
+    """The binding's device status word for ``device`` (an int32 tensor); a
+    bare "cuda" means the current CUDA device, as it does for tensors."""
     device = torch.device(device)
+    if device.type == "cuda" and device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
     if device not in _status:
         _status[device] = torch.zeros(1, dtype=torch.int32, device=device)
     return _status[device]
