@@ -6,6 +6,7 @@ it is given), and pass raw pointers and the current CUDA stream.  Every step
 of the boundary runs in the library's CUDA kernels; there is no fallback: if
 the library is not built, ``load()`` raises.
 """
+import contextlib
 import ctypes
 import os
 
@@ -116,6 +117,11 @@ def _ptr_array(ts):
     return ctypes.cast(arr, _PP)
 
 
+def _on_device(device):
+    """The calls launch on the current CUDA device: make it the tensors' own."""
+    return torch.cuda.device(device) if device.type == "cuda" else contextlib.nullcontext()
+
+
 def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -224,12 +230,13 @@ def _rs_norm_fwd_call(entry, mask_div, partials, residual, bias, gamma, beta, ep
         _need(beta, (h,), bf, dev, "beta")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    code = getattr(lib, entry)(
-        _ptr_array(partials), _ptr_array(residual), _ptr(bias), _ptr(gamma),
-        _ptr(beta) if ln else None, b, s, h, t, float(eps), float(p), int(seed), int(offset),
-        cu, n_seqs, NORMS[norm], _ptr_array(z_out), _ptr_array(mask_out),
-        _ptr_array(mean_out) if ln else None, _ptr_array(rstd_out), _ptr_array(gathered),
-        len(gathered), _ptr(st), _stream(dev))
+    with _on_device(dev):
+        code = getattr(lib, entry)(
+            _ptr_array(partials), _ptr_array(residual), _ptr(bias), _ptr(gamma),
+            _ptr(beta) if ln else None, b, s, h, t, float(eps), float(p), int(seed), int(offset),
+            cu, n_seqs, NORMS[norm], _ptr_array(z_out), _ptr_array(mask_out),
+            _ptr_array(mean_out) if ln else None, _ptr_array(rstd_out), _ptr_array(gathered),
+            len(gathered), _ptr(st), _stream(dev))
     _check(code)
 
 
@@ -260,12 +267,13 @@ def sp_shard_norm_fwd(y_shards, residual, bias, gamma, beta, *, s, eps, p, seed,
         _need(beta, (h,), bf, dev, "beta")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    _check(lib.sp_shard_norm_fwd(
-        _ptr_array(y_shards), _ptr_array(residual), _ptr(bias), _ptr(gamma),
-        _ptr(beta) if ln else None, b, s, h, t, float(eps), float(p), int(seed), int(offset),
-        cu, n_seqs, NORMS[norm], _ptr_array(z_out), _ptr_array(mask_out),
-        _ptr_array(mean_out) if ln else None, _ptr_array(rstd_out), _ptr_array(o_shards),
-        _ptr(st), _stream(dev)))
+    with _on_device(dev):
+        _check(lib.sp_shard_norm_fwd(
+            _ptr_array(y_shards), _ptr_array(residual), _ptr(bias), _ptr(gamma),
+            _ptr(beta) if ln else None, b, s, h, t, float(eps), float(p), int(seed), int(offset),
+            cu, n_seqs, NORMS[norm], _ptr_array(z_out), _ptr_array(mask_out),
+            _ptr_array(mean_out) if ln else None, _ptr_array(rstd_out), _ptr_array(o_shards),
+            _ptr(st), _stream(dev)))
 
 
 def sp_allgather_seq(shards, gathered, *, s, cu_seqlens=None, status=None):
@@ -281,8 +289,9 @@ def sp_allgather_seq(shards, gathered, *, s, cu_seqlens=None, status=None):
         _need(g, (b, s, h), torch.bfloat16, dev, f"gathered[{j}]")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    _check(lib.sp_allgather_seq(_ptr_array(shards), b, s, h, t, cu, n_seqs,
-                                _ptr_array(gathered), len(gathered), _ptr(st), _stream(dev)))
+    with _on_device(dev):
+        _check(lib.sp_allgather_seq(_ptr_array(shards), b, s, h, t, cu, n_seqs,
+                                    _ptr_array(gathered), len(gathered), _ptr(st), _stream(dev)))
 
 
 def sp_reduce_scatter_seq(partials, shards, *, cu_seqlens=None, status=None):
@@ -297,8 +306,9 @@ def sp_reduce_scatter_seq(partials, shards, *, cu_seqlens=None, status=None):
         _need(shards[r], (b, sizes[r], h), torch.bfloat16, dev, f"shards[{r}]")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    _check(lib.sp_reduce_scatter_seq(_ptr_array(partials), b, s, h, t, cu, n_seqs,
-                                     _ptr_array(shards), _ptr(st), _stream(dev)))
+    with _on_device(dev):
+        _check(lib.sp_reduce_scatter_seq(_ptr_array(partials), b, s, h, t, cu, n_seqs,
+                                         _ptr_array(shards), _ptr(st), _stream(dev)))
 
 
 def sp_norm_bwd_workspace_bytes(b, s, h, t, norm="layernorm"):
@@ -353,12 +363,13 @@ def _norm_bwd_call(entry, mask_div, dy, z, mask, mean, rstd, gamma, dz_skip, s, 
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    code = getattr(lib, entry)(
-        _ptr_array(dy), _ptr_array(z), _ptr_array(mask), _ptr_array(mean) if ln else None,
-        _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), cu, n_seqs,
-        NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
-        _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev))
+    with _on_device(dev):
+        code = getattr(lib, entry)(
+            _ptr_array(dy), _ptr_array(z), _ptr_array(mask), _ptr_array(mean) if ln else None,
+            _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), cu, n_seqs,
+            NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
+            _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev))
     _check(code)
 
 
@@ -413,13 +424,14 @@ def _rs_norm_bwd_call(entry, mask_div, dy_partials, z, mask, mean, rstd, gamma, 
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    _check(getattr(lib, entry)(
-        _ptr_array(dy_partials), _ptr_array(z), _ptr_array(mask),
-        _ptr_array(mean) if ln else None, _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip),
-        b, s, h, t, float(p), cu, n_seqs, NORMS[norm], _ptr_array(dresidual),
-        _ptr_array(dgathered), len(dgathered), _ptr(dgamma), _ptr(dbeta) if ln else None,
-        _ptr(dbias), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(st),
-        _stream(dev)))
+    with _on_device(dev):
+        _check(getattr(lib, entry)(
+            _ptr_array(dy_partials), _ptr_array(z), _ptr_array(mask),
+            _ptr_array(mean) if ln else None, _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip),
+            b, s, h, t, float(p), cu, n_seqs, NORMS[norm], _ptr_array(dresidual),
+            _ptr_array(dgathered), len(dgathered), _ptr(dgamma), _ptr(dbeta) if ln else None,
+            _ptr(dbias), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(st),
+            _stream(dev)))
 
 
 def sp_norm_bwd_philox(dy, z, mean, rstd, gamma, dz_skip=None, *, s, p, seed, offset=0,
@@ -452,12 +464,13 @@ def sp_norm_bwd_philox(dy, z, mean, rstd, gamma, dz_skip=None, *, s, p, seed, of
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    _check(lib.sp_norm_bwd_philox(
-        _ptr_array(dy), _ptr_array(z), _ptr_array(mean) if ln else None, _ptr_array(rstd),
-        _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), int(seed), int(offset), cu,
-        n_seqs, NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
-        _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev)))
+    with _on_device(dev):
+        _check(lib.sp_norm_bwd_philox(
+            _ptr_array(dy), _ptr_array(z), _ptr_array(mean) if ln else None, _ptr_array(rstd),
+            _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), int(seed), int(offset), cu,
+            n_seqs, NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
+            _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(st), _stream(dev)))
 
 
 NOALLOC_WORKSPACE_BYTES = 16 << 20
@@ -500,11 +513,12 @@ def sp_norm_bwd_noalloc(dy, z, mask, mean, rstd, gamma, dz_skip=None, *, s, p, c
             _need(v, (h,), torch.float32, dev, name)
     cu, n_seqs = _seq_meta(cu_seqlens, b, dev)
     st = device_status(dev) if status is None else status
-    code = lib.sp_norm_bwd_noalloc(
-        _ptr_array(dy), _ptr_array(z), _ptr_array(mask), _ptr_array(mean) if ln else None,
-        _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), cu, n_seqs,
-        NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
-        _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(st), _stream(dev))
+    with _on_device(dev):
+        code = lib.sp_norm_bwd_noalloc(
+            _ptr_array(dy), _ptr_array(z), _ptr_array(mask), _ptr_array(mean) if ln else None,
+            _ptr_array(rstd), _ptr(gamma), _ptr_array(dz_skip), b, s, h, t, float(p), cu, n_seqs,
+            NORMS[norm], _ptr_array(dresidual), _ptr_array(dgathered), len(dgathered),
+            _ptr(dgamma), _ptr(dbeta) if ln else None, _ptr(dbias), _ptr(st), _stream(dev))
     _check(code)
 
 
