@@ -75,6 +75,13 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
 #pragma unroll
   for (int ch = 0; ch < MAXC; ++ch)
     if (ch < nchunk && ch * kChunk + c0 < h) valid |= 1u << ch;
+  // BITS: lane l < 8 of warp w copies bytes [32 w + 4 l, 32 w + 4 l + 4) of
+  // each chunk's NTHR mask bytes; bit ch: that piece lies inside the row
+  const int bits_lane = (tid & ~31) + 4 * (tid & 31);
+  uint32_t bits_copy = 0;
+#pragma unroll
+  for (int ch = 0; ch < MAXC; ++ch)
+    if (BITS && (tid & 31) < 8 && ch * NTHR + bits_lane < h / 8) bits_copy |= 1u << ch;
 
   if (blockIdx.x == 0 && tid < 32) check_cu_seqlens(P.cu_seqlens, P.n_seqs, P.rows, P.status);
 
@@ -117,13 +124,10 @@ __global__ void __launch_bounds__(NTHR, bwd_tmem_shape(NTHR, MAXC)
           if (!REGEN && !BITS) cp_async8(it + off_mask - tid * 8, mp + ch * kChunk);   // 8 B apart
           if (has_skip) cp_async16(it + off_skip, P.dz_skip[k] + lo0 + ch * kChunk);
         }
-        if (BITS && (tid & 31) < 8) {
-          // bytes [4 l, 4 l + 4) of this warp's 32 (lane l); with h % 32 == 0
-          // a 4-byte piece is wholly inside the row or wholly past its end
-          const int byte0 = ch * NTHR + (tid & ~31) + 4 * (tid & 31);
-          if (byte0 < h / 8)
-            cp_async4(it0 - tid * 16 + ch * item_bytes + off_mask + (byte0 - ch * NTHR),
-                      P.mask[k] + (pw.local * h) / 8 + byte0);
+        if (BITS && ((bits_copy >> ch) & 1u)) {
+          // (h % 32 == 0: a 4-byte piece is wholly inside the row or past it)
+          cp_async4(it0 - tid * 16 + ch * item_bytes + off_mask + bits_lane,
+                    P.mask[k] + (static_cast<uint64_t>(pw.local) * h >> 3) + ch * NTHR + bits_lane);
         }
       }
       rec.row = pw.row;
