@@ -202,3 +202,54 @@ def test_dependent_calls_back_to_back_and_in_a_graph_equal_synchronised_calls(va
         torch.cuda.synchronize()
         sp.check_device_status(C.DEV)
         assert _same(ref, _snapshot(sets)), f"graph replay {rep}"
+
+
+def test_independent_calls_on_separate_streams_equal_serial_calls():
+    """Three independent problems (their own inputs, outputs and workspaces),
+    each forward + backward on a stream of its own, forked from and joined to
+    the current stream as the bench runs length buckets: the bits of the same
+    calls run one after another."""
+    shapes = [dict(t=8, b=1, s=1024, h=4096), dict(t=4, b=1, s=2048, h=5120,
+                                                    seqlens=(700, 1, 1200, 147)),
+              dict(t=8, b=2, s=512, h=8192, norm="rmsnorm", eps=1e-6)]
+    ws_ = [wl.Workload(f"par{i}", draw_seed=600 + i, **v) for i, v in enumerate(shapes)]
+    inps = [wl.forward_inputs(w, C.DEV) for w in ws_]
+    dys = [wl.backward_inputs(w, C.DEV)["dy"] for w in ws_]
+    cus = [torch.from_numpy(wl.cu_seqlens(w.seqlens)).to(C.DEV) if w.ragged else None
+           for w in ws_]
+
+    def run_all(streams):
+        outs = []
+        main = torch.cuda.current_stream(C.DEV)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        joins = []
+        for i, w in enumerate(ws_):
+            f = C.alloc_fwd(w, 1, fill=7.0)
+            b = C.alloc_bwd(w, 1)
+            stream = streams[i] if streams else main
+            stream.wait_event(fork)
+            with torch.cuda.stream(stream):
+                C.run_fwd(w, inps[i], n_gather=1, out=f, cu_seqlens=cus[i])
+                C.run_bwd(w, f, inps[i]["gamma"], dys[i], None, n_gather=1, out=b,
+                          cu_seqlens=cus[i])
+                done = torch.cuda.Event()
+                done.record(stream)
+            joins.append(done)
+            outs.append((f, b))
+        for done in joins:
+            main.wait_event(done)
+        torch.cuda.synchronize()
+        C.sp.check_device_status(C.DEV)
+        return outs
+
+    serial = run_all(None)
+    streams = [torch.cuda.Stream(C.DEV) for _ in ws_]
+    for rep in range(3):
+        par = run_all(streams)
+        for w, (fs, bs), (fp, bp) in zip(ws_, serial, par):
+            for key in ("z", "mask", "rstd", "gathered") + (("mean",) if w.norm == "layernorm"
+                                                             else ()):
+                for a, b in zip(fs[key], fp[key]):
+                    assert C.bits_equal(a, b), (w.name, key, rep)
+            C.assert_bwd_outputs_equal(w, bs, bp)
