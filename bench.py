@@ -253,9 +253,10 @@ def profiled_traffic():
 
 def profiled_workload(args):
     """The recorded traffic belongs to the default bench line only (70B shape,
-    LayerNorm, p = 0.1, one gathered copy, no size overrides)."""
+    LayerNorm, p = 0.1, one gathered copy, the byte mask, no size overrides)."""
     return (args.workload == "70b" and not args.s and not args.h and args.p is None
-            and args.norm in (None, "layernorm") and args.n_gather == 1)
+            and args.norm in (None, "layernorm") and args.n_gather == 1
+            and args.mask == "stored")
 
 
 class Step:

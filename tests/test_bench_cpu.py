@@ -69,3 +69,15 @@ def test_bucketed_step_covers_the_batch(lib):
 def test_step_bytes_of_each_mask_mode(mask, entry, fwd, bwd):
     w = wl.WORKLOADS["70b"]
     assert bench.step_bytes_per_token(w, 1, "fused", mask, entry) == (fwd, bwd)
+
+
+def test_recorded_traffic_belongs_to_the_default_line_only():
+    """The profiled DRAM traffic is that of the default line's forward kernel:
+    a line whose forward is another kernel (another mask format, workload,
+    norm or number of gathered copies) reports none."""
+    base = dict(workload="70b", s=0, h=0, p=None, norm=None, n_gather=1, mask="stored")
+    ns = lambda **kw: type("A", (), {**base, **kw})
+    assert bench.profiled_workload(ns())
+    for change in (dict(mask="bits"), dict(mask="regen"), dict(workload="ragged"),
+                   dict(norm="rmsnorm"), dict(n_gather=8), dict(s=2048), dict(p=0.0)):
+        assert not bench.profiled_workload(ns(**change)), change
