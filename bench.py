@@ -777,10 +777,14 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: {norm_name} boundary fwd+bwd, t={w.t} emulated ranks, "
                                f"b={w.b}, s={w.s}, h={w.h}, p={w.p}, n_gather={args.n_gather}"
                                + (f", {len(buckets)} length buckets (max_cv={args.max_cv}), "
-                                  "one call pair per bucket" if buckets else ""),
+                                  "one call pair per bucket, each bucket on a stream of its own"
+                                  if buckets else ""),
                    "t": w.t, "b": w.b, "s": w.s, "h": w.h, "norm": w.norm, "p": w.p,
                    "n_gather": args.n_gather, "pipeline": args.pipeline,
                    "backward_mask": args.mask, "backward_entry": args.bwd_entry,
+                   "mask_storage": {"stored": "1 byte per element",
+                                    "bits": "1 bit per element",
+                                    "regen": "none (the backward draws it again)"}[args.mask],
                    "launch": f"cuda graphs of {min(GRAPH_STEPS, args.steps)} steps (each step "
                              "its forward and backward calls); the fwd/bwd split from a second "
                              "loop with one graph per call"
