@@ -185,3 +185,28 @@ def test_rs_norm_bwd_bit_mask_full_size_equals_byte_mask():
     torch.cuda.synchronize()
     C.sp.check_device_status(C.DEV)
     C.assert_bwd_outputs_equal(w, ref, got)
+
+
+def test_tensors_beyond_2_31_elements():
+    """Tensors of more than 2^31 elements (t = 2, s = 266,240 tokens of
+    h = 8192: 2.18 G elements per partial, about 38 GB in all): every element
+    of rows on both sides of element 2^31 (token 262,144), of the shard
+    boundary and of the first and last rows, forward and backward, against
+    the oracle -- the kernels' 64-bit index arithmetic."""
+    import numpy as np
+    w = wl.Workload("big", t=2, b=1, s=266240, h=8192, draw_seed=77)
+    assert w.s * w.h > 2 ** 31
+    inp = wl.forward_inputs(w, C.DEV)
+    fwd = C.run_fwd(w, inp, n_gather=1)
+    dy = wl.backward_inputs(w, C.DEV)["dy"]
+    bwd = C.run_bwd(w, fwd, inp["gamma"], dy, None, n_gather=1)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    edge = 2 ** 31 // w.h
+    tokens = np.array(sorted({0, 1, edge - 2, edge - 1, edge, edge + 1, w.s // 2 - 1, w.s // 2,
+                              w.s - 2, w.s - 1} | set(range(edge - 8, edge + 8, 3))),
+                      dtype=np.int64)
+    C.check_fwd_rows(w, inp, fwd, tokens)
+    C.check_bwd_rows(w, fwd, inp["gamma"], dy, None, bwd, tokens)
+    for name in ("dgamma", "dbeta", "dbias"):
+        assert torch.isfinite(bwd[name]).all(), name
