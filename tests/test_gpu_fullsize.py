@@ -192,7 +192,8 @@ def test_tensors_beyond_2_31_elements():
     h = 8192: 2.18 G elements per partial, about 38 GB in all): every element
     of rows on both sides of element 2^31 (token 262,144), of the shard
     boundary and of the first and last rows, forward and backward, against
-    the oracle -- the kernels' 64-bit index arithmetic."""
+    the oracle -- the kernels' 64-bit index arithmetic; and the bit-mask pair
+    on the same inputs, bit for bit the byte-mask pair on every element."""
     import numpy as np
     w = wl.Workload("big", t=2, b=1, s=266240, h=8192, draw_seed=77)
     assert w.s * w.h > 2 ** 31
@@ -210,3 +211,8 @@ def test_tensors_beyond_2_31_elements():
     C.check_bwd_rows(w, fwd, inp["gamma"], dy, None, bwd, tokens)
     for name in ("dgamma", "dbeta", "dbias"):
         assert torch.isfinite(bwd[name]).all(), name
+    # the bit-packed mask at this size: every output of the pair bit for bit
+    fwd_k, bwd_k = C.run_bitmask_pair(w, inp, dy, None, 1, 1)
+    torch.cuda.synchronize()
+    C.sp.check_device_status(C.DEV)
+    C.assert_bitmask_pair_matches(w, fwd, bwd, fwd_k, bwd_k)
